@@ -1,0 +1,202 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module is shared by the tests, the benchmark and the oracle's checks.  It
+only draws random numbers and lays out raw storage bits: sequence lengths,
+query/key/value values (drawn in fp32 from N(0, 1) and rounded to fp16 or bf16
+storage bits), shuffled free-block orders and NaN poison patterns.  It holds
+none of the attention, address-translation, cache-write or block-copy
+arithmetic; those live, separately, in the CUDA library and in the oracle.
+
+The workload shapes follow the five decode workloads this library is
+measured on (tiny, Llama-3-8B-shaped, shared prefix, long context, ragged
+continuous-batching step).  The sequence-length mixes follow the pages:
+uniform ranges for the fixed-batch workloads, and a lognormal length mix for
+the continuous-batching step (the simulator exercise of the Paged Attention
+tutorial, §10 "Hands-on exercise", draws request lengths from a lognormal).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+# Storage dtype codes, identical to the C ABI's pa_dtype enumeration.
+FLOAT16 = 0
+BFLOAT16 = 1
+DTYPE_NAMES = {FLOAT16: "f16", BFLOAT16: "bf16"}
+
+# Quiet-NaN bit patterns used to poison unused slots and unused blocks.
+NAN_BITS = {FLOAT16: 0x7E00, BFLOAT16: 0x7FC0}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """Shape and length distribution of one synthetic decode workload."""
+
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    dtype: int
+    seed: int
+    # length distribution: "fixed" (lens), "uniform" (lo..hi inclusive),
+    # "lognormal" (median, sigma, clipped to lo..hi), "shared_prefix"
+    length_kind: str
+    lens: tuple = ()
+    lo: int = 1
+    hi: int = 1
+    median: float = 0.0
+    sigma: float = 0.0
+    num_blocks: int = 0          # 0: pool_factor x the blocks the batch needs
+    pool_factor: float = 1.25
+    partition_tokens: int = 512
+    # shared-prefix workload
+    num_prompts: int = 0
+    samples_per_prompt: int = 0
+    prefix_tokens: int = 0
+    prefix_jitter: int = 0       # extra prompt tokens drawn from U{0..jitter}
+    tail_lo: int = 0
+    tail_hi: int = 0
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def scale(self) -> float:
+        """Softmax scale 1/sqrt(head_dim), as the fp32 value a kernel receives."""
+        return float(np.float32(1.0 / math.sqrt(self.head_dim)))
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2
+
+    def with_block_size(self, bs: int) -> "Workload":
+        return dataclasses.replace(self, block_size=bs, name=f"{self.name}_bs{bs}")
+
+
+TINY = Workload(
+    name="tiny", num_seqs=4, num_q_heads=4, num_kv_heads=4, head_dim=64,
+    block_size=16, dtype=FLOAT16, seed=0, length_kind="fixed",
+    lens=(5, 16, 37, 64), num_blocks=32)
+
+LLAMA3_8B = Workload(
+    name="llama3_8b", num_seqs=64, num_q_heads=32, num_kv_heads=8, head_dim=128,
+    block_size=16, dtype=BFLOAT16, seed=1, length_kind="uniform", lo=128, hi=4096)
+
+SHARED_PREFIX = Workload(
+    name="shared_prefix", num_seqs=128, num_q_heads=32, num_kv_heads=8,
+    head_dim=128, block_size=16, dtype=BFLOAT16, seed=2, length_kind="shared_prefix",
+    num_prompts=16, samples_per_prompt=8, prefix_tokens=2048, prefix_jitter=15,
+    tail_lo=0, tail_hi=512)
+
+LONG_CONTEXT = Workload(
+    name="long_context", num_seqs=8, num_q_heads=64, num_kv_heads=8, head_dim=128,
+    block_size=32, dtype=BFLOAT16, seed=3, length_kind="uniform", lo=32768, hi=131072)
+
+RAGGED = Workload(
+    name="ragged", num_seqs=256, num_q_heads=32, num_kv_heads=8, head_dim=128,
+    block_size=16, dtype=BFLOAT16, seed=4, length_kind="lognormal",
+    median=512.0, sigma=1.0, lo=1, hi=8192)
+
+RAGGED_BLOCK_SIZES = (8, 16, 32, 64)
+
+WORKLOADS = {w.name: w for w in (TINY, LLAMA3_8B, SHARED_PREFIX, LONG_CONTEXT, RAGGED)}
+
+
+# ----------------------------------------------------------------------------
+# random streams
+# ----------------------------------------------------------------------------
+
+_STREAMS = {"lens": 1, "values": 2, "free": 3, "query": 4, "new_kv": 5, "tails": 6}
+
+
+def rng(w: Workload, stream: str, sub: int = 0) -> np.random.Generator:
+    """Independent PCG64 stream per (workload seed, purpose, sub-index)."""
+    return np.random.default_rng([w.seed, _STREAMS[stream], sub])
+
+
+def seq_lens(w: Workload) -> np.ndarray:
+    """Draw the per-sequence context lengths of a fixed-batch workload."""
+    g = rng(w, "lens")
+    if w.length_kind == "fixed":
+        return np.asarray(w.lens, dtype=np.int64)
+    if w.length_kind == "uniform":
+        return g.integers(w.lo, w.hi + 1, size=w.num_seqs, dtype=np.int64)
+    if w.length_kind == "lognormal":
+        z = g.standard_normal(w.num_seqs)
+        raw = np.rint(np.exp(math.log(w.median) + w.sigma * z))
+        return np.clip(raw, w.lo, w.hi).astype(np.int64)
+    raise ValueError(f"{w.name}: lengths of kind {w.length_kind!r} are drawn per prompt")
+
+
+def prompt_extra_tokens(w: Workload) -> np.ndarray:
+    """Shared-prefix workload: extra prompt tokens k_p ~ U{0..jitter} per prompt."""
+    return rng(w, "lens").integers(0, w.prefix_jitter + 1, size=w.num_prompts, dtype=np.int64)
+
+
+def sample_tail_lens(w: Workload) -> np.ndarray:
+    """Shared-prefix workload: generated tokens per sample, U{tail_lo..tail_hi}."""
+    return rng(w, "tails").integers(
+        w.tail_lo, w.tail_hi + 1, size=(w.num_prompts, w.samples_per_prompt), dtype=np.int64)
+
+
+def shuffled_free_order(num_blocks: int, g: np.random.Generator) -> list:
+    """A seeded permutation of the block ids [0, num_blocks), used as the
+    initial free stack so that allocations come out scattered."""
+    return [int(x) for x in g.permutation(num_blocks)]
+
+
+# ----------------------------------------------------------------------------
+# storage bits
+# ----------------------------------------------------------------------------
+
+def fp32_to_storage_bits(x: np.ndarray, dtype: int) -> np.ndarray:
+    """Round fp32 values to fp16/bf16 (round to nearest even) and return the
+    raw 16-bit patterns as uint16."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == FLOAT16:
+        return x.astype(np.float16).view(np.uint16)
+    if dtype == BFLOAT16:
+        u = x.view(np.uint32)
+        nan = np.isnan(x)
+        # finite values and infinities stay below 2^32 after the bias
+        safe = np.where(nan, np.uint32(0), u)
+        bits = ((safe + np.uint32(0x7FFF) + ((safe >> 16) & np.uint32(1))) >> 16).astype(np.uint16)
+        if nan.any():
+            bits[nan] = NAN_BITS[BFLOAT16]
+        return bits
+    raise ValueError(f"unknown dtype code {dtype}")
+
+
+def normal_bits(g: np.random.Generator, shape: Sequence[int], dtype: int) -> np.ndarray:
+    """N(0, 1) values drawn in fp32 and rounded to storage bits."""
+    return fp32_to_storage_bits(g.standard_normal(size=tuple(shape), dtype=np.float32), dtype)
+
+
+def nan_bits(shape: Sequence[int], dtype: int) -> np.ndarray:
+    return np.full(tuple(shape), NAN_BITS[dtype], dtype=np.uint16)
+
+
+def query_bits(w: Workload, num_seqs: Optional[int] = None, sub: int = 0) -> np.ndarray:
+    b = w.num_seqs if num_seqs is None else num_seqs
+    return normal_bits(rng(w, "query", sub), (b, w.num_q_heads, w.head_dim), w.dtype)
+
+
+def token_kv_bits(w: Workload, num_tokens: int, sub: int) -> tuple:
+    """K and V storage bits for `num_tokens` tokens: two [T, Hkv, D] uint16 arrays."""
+    g = rng(w, "values", sub)
+    shape = (num_tokens, w.num_kv_heads, w.head_dim)
+    return normal_bits(g, shape, w.dtype), normal_bits(g, shape, w.dtype)
+
+
+def pool_fill_bits(w: Workload, num_blocks: int, sub: int = 0) -> tuple:
+    """A whole pool of random K and V bits, [NB, bs, Hkv, D] each (used where the
+    values of every slot are random data rather than specific tokens)."""
+    g = rng(w, "values", 10_000 + sub)
+    shape = (num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    return normal_bits(g, shape, w.dtype), normal_bits(g, shape, w.dtype)
