@@ -1,0 +1,570 @@
+"""Benchmark: one decode step of paged attention per timed step, on GB300.
+
+A step is the whole hot path over one batch: the slot of each sequence's newest
+token (pa_decode_slots), the cache write of that token's K/V
+(pa_reshape_and_cache), copy-on-write block copies when the workload shares
+blocks (pa_copy_blocks), and decode attention over the paged pool (pa_decode:
+split-K main kernel + combine).  Inputs are synthetic and seeded; the pool is
+resident in HBM before timing starts.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload on its own GPU (the path has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and decode tokens/s, 1 GPU"
+L2_BYTES = 126 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------
+# workload description shared by both arms
+# ----------------------------------------------------------------------------
+
+def workload(name: str, block_size: int | None):
+    w = syn.WORKLOADS[name]
+    if block_size:
+        w = w.with_block_size(block_size)
+    return w
+
+
+def kv_bytes(lens, w) -> int:
+    """Algorithmic K+V bytes one decode reads: every token once per KV head."""
+    return int(np.sum(lens)) * w.num_kv_heads * w.head_dim * 2 * w.elem_bytes
+
+
+def decode_bytes(lens, w, max_blocks) -> int:
+    """Algorithmic bytes of one pa_decode launch: K/V once per KV head, q read,
+    out written, the table entries of every block used, seq_lens."""
+    B = len(lens)
+    qo = 2 * B * w.num_q_heads * w.head_dim * w.elem_bytes
+    blocks = int(np.sum([-(-int(L) // w.block_size) for L in lens]))
+    return kv_bytes(lens, w) + qo + 4 * blocks + 4 * B
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_uuid(torch, dev) -> str | None:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# native arm
+# ----------------------------------------------------------------------------
+
+def kernel_sources_sha() -> str:
+    csrc = os.path.join(ROOT, "paged_kv_cache_301_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per pa_decode launch from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = kernel_sources_sha()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == workload_name and parts[1] == sha:
+            return float(parts[2])
+    return None
+
+
+class NativeStep:
+    """Device state of one replica: pool, tables, inputs; run() = one step."""
+
+    def __init__(self, pa, torch, w, dev, partition_tokens: int):
+        self.pa, self.torch, self.w, self.dev = pa, torch, w, dev
+        bs = w.block_size
+        lens = syn.seq_lens(w)
+        B = len(lens)
+        blocks = sum(-(-int(L) // bs) for L in lens)
+        nb = int(math.ceil(w.pool_factor * blocks)) + 1
+        bm = pa.BlockManager(nb, bs, syn.shuffled_free_order(nb, syn.rng(w, "free")))
+        pad = bm.allocate(1)[0]
+        seqs = []
+        for L in lens:
+            s = bm.new_sequence(int(L) - 1)     # context before this step
+            bm.append(s)                        # the step's token: opens a block at a boundary
+            seqs.append(s)
+        mb = max(bm.seq_num_blocks(s) for s in seqs)
+        tables, seq_lens = bm.export(seqs, mb, pad)
+        self.lens = lens
+        self.max_blocks = mb
+        self.num_blocks = nb
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed)
+        tdt = torch.bfloat16 if w.dtype == syn.BFLOAT16 else torch.float16
+        shape = (nb, bs, w.num_kv_heads, w.head_dim)
+        self.k_pool = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(tdt)
+        self.v_pool = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(tdt)
+        self.q = torch.randn((B, w.num_q_heads, w.head_dim), generator=g, device=dev).to(tdt)
+        self.key = torch.randn((B, w.num_kv_heads, w.head_dim), generator=g, device=dev).to(tdt)
+        self.value = torch.randn_like(self.key)
+        self.tables = tables.to(dev)
+        self.seq_lens = seq_lens.to(dev)
+        self.slots = torch.empty(B, dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.max_seq_len = int(lens.max())
+        self.pt = partition_tokens
+        self.ws = pa.alloc_workspace(B, w.num_q_heads, w.head_dim, self.max_seq_len,
+                                     partition_tokens, dev)
+        P = -(-self.max_seq_len // (partition_tokens or 512))
+        self.launches_per_step = 3 + (1 if P > 1 else 0)
+        # pinned host copies for the end-to-end measurement
+        self.h_q = self.q.cpu().pin_memory()
+        self.h_key = self.key.cpu().pin_memory()
+        self.h_value = self.value.cpu().pin_memory()
+        self.h_tables = self.tables.cpu().pin_memory()
+        self.h_lens = self.seq_lens.cpu().pin_memory()
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in
+                             (self.h_q, self.h_key, self.h_value, self.h_tables, self.h_lens))
+        self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
+
+    def write_step(self):
+        pa = self.pa
+        pa.pa_decode_slots(self.slots, self.tables, self.seq_lens, self.w.block_size)
+        pa.pa_reshape_and_cache(self.k_pool, self.v_pool, self.key, self.value, self.slots)
+
+    def decode(self):
+        self.pa.pa_decode(self.out, self.q, self.k_pool, self.v_pool, self.tables, self.seq_lens,
+                          self.w.scale, max_seq_len=self.max_seq_len,
+                          partition_tokens=self.pt, workspace=self.ws)
+
+    def run(self):
+        self.write_step()
+        self.decode()
+
+    def run_e2e(self):
+        # step inputs from pinned host memory, result back to pinned host memory
+        self.q.copy_(self.h_q, non_blocking=True)
+        self.key.copy_(self.h_key, non_blocking=True)
+        self.value.copy_(self.h_value, non_blocking=True)
+        self.tables.copy_(self.h_tables, non_blocking=True)
+        self.seq_lens.copy_(self.h_lens, non_blocking=True)
+        self.run()
+        self.h_out.copy_(self.out, non_blocking=True)
+
+
+def run_native(args, dist_info):
+    import torch
+    import paged_kv_cache_301_gb300 as pa
+    from paged_kv_cache_301_gb300 import build as _build
+
+    rank, world, local = dist_info
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workload(args.workload, args.block_size)
+    cpu_baseline = None
+    if rank == 0 and not args.no_cpu_baseline:
+        # before the first GPU call: the oracle's pool is a spawn pool anyway
+        cpu_baseline = cpu_oracle_baseline(w, budget_s=args.cpu_budget)
+    step = NativeStep(pa, torch, w, dev, args.partition_tokens)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_uuid(torch, dev))
+    clocks.start()
+    time.sleep(0.25)           # let the sampler take its first reading
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step.write_step()
+        ev[i][0].record(stream)
+        step.decode()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    decode_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # end to end: host buffers in, host result out, every step
+    for _ in range(max(3, args.warmup // 4)):
+        step.run_e2e()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.run_e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    ms_step = total_ms / args.steps
+    kvb = kv_bytes(step.lens, w)
+    B = len(step.lens)
+    value = world * kvb / (ms_step * 1e-3) / 1e9
+    dec_avg_ms = sum(decode_ms) / len(decode_ms)
+    dec_bytes = decode_bytes(step.lens, w, step.max_blocks)
+    peak, peak_kind = measured_peaks()
+    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(w.name)
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": syn.DTYPE_NAMES[w.dtype],
+        "data": "synthetic (seeded N(0,1) q/K/V; block ids a seeded permutation)",
+        "config": {
+            "workload": w.name, "num_seqs": B, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "seq_lens": f"{w.length_kind} [{w.lo},{w.hi}]"
+            if w.length_kind != "fixed" else list(w.lens),
+            "total_tokens": int(np.sum(step.lens)), "num_blocks": step.num_blocks,
+            "partition_tokens": args.partition_tokens or 512,
+            "kv_bytes_per_step": kvb,
+            "l2": f"inputs larger than L2: {kvb / 2**20:.0f} MiB of K/V read per step vs "
+                  f"{L2_BYTES / 2**20:.0f} MiB L2; no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
+        "kv_frac_of_peak": round(value / world / peak, 4),
+        "wall_s": round(wall, 4),
+        "e2e": {
+            "value": round(world * kvb / (e2e_ms / args.steps * 1e-3) / 1e9, 1),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms / args.steps, 5),
+            "h2d_bytes_per_step": step.h2d_bytes,
+            "d2h_bytes_per_step": step.d2h_bytes,
+        },
+        "gpu_launches": step.launches_per_step * args.steps,
+        "roofline": {
+            "kernel": "pa_decode (split-K main + combine)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes": dec_bytes,
+            "avg_launch_ms": round(dec_avg_ms, 5),
+        },
+        "clocks": clk,
+        "cpu_baseline": cpu_baseline,
+    }
+    return result
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+_shared = {}
+
+
+def _pool_init(spec):
+    from multiprocessing import shared_memory
+    for key, (name, shape, dtype) in spec.items():
+        shm = shared_memory.SharedMemory(name=name)
+        _shared[key] = (shm, np.ndarray(shape, dtype=np.dtype(dtype), buffer=shm.buf))
+
+
+def _pool_task(args):
+    b, scale, dtype, heads = args
+    from oracle.attention import paged_decode_attention
+    out = paged_decode_attention(_shared["q"][1], _shared["k"][1], _shared["v"][1],
+                                 _shared["tables"][1], _shared["lens"][1], scale,
+                                 sequences=[b], heads=heads, dtype=dtype)
+    return float(out[b].sum())
+
+
+class OraclePool:
+    """The fp64 oracle over a host copy of the workload, run on a spawn pool with
+    one single-threaded worker per host core."""
+
+    def __init__(self, w, cores=None):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        from oracle import scenarios
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        self.batch = scenarios.fixed_batch(w)
+        b = self.batch
+        arrays = {"q": b.q, "k": b.k_pool, "v": b.v_pool,
+                  "tables": b.block_tables.astype(np.int32),
+                  "lens": b.seq_lens.astype(np.int32)}
+        self.shms = []
+        spec = {}
+        for key, arr in arrays.items():
+            shm = shared_memory.SharedMemory(create=True, size=max(arr.nbytes, 1))
+            view = np.ndarray(arr.shape, dtype=arr.dtype, buffer=shm.buf)
+            view[...] = arr
+            self.shms.append(shm)
+            spec[key] = (shm.name, arr.shape, arr.dtype.str)
+        self.cores = cores or len(os.sched_getaffinity(0))
+        ctx = mp.get_context("spawn")
+        self.pool = ctx.Pool(self.cores, initializer=_pool_init, initargs=(spec,))
+        self.pool.map(_pool_task, [(0, b.scale, b.dtype, [0])] * self.cores)   # warm the workers
+        self.w = w
+
+    def run(self, units):
+        """units: list of (b, heads); returns seconds."""
+        t0 = time.perf_counter()
+        self.pool.map(_pool_task, [(b, self.batch.scale, self.batch.dtype, heads)
+                                   for b, heads in units], chunksize=1)
+        return time.perf_counter() - t0
+
+    def unit_bytes(self, units):
+        w = self.w
+        G = w.group
+        lens = self.batch.seq_lens
+        # K/V bytes the oracle reads: per query head it gathers its KV head's rows
+        return sum(int(lens[b]) * w.head_dim * 2 * w.elem_bytes * len(heads) / G
+                   for b, heads in units)
+
+    def close(self):
+        self.pool.terminate()
+        for s in self.shms:
+            s.close()
+            s.unlink()
+
+
+def cpu_oracle_baseline(w, budget_s=15.0):
+    """Oracle throughput on the host cores: whole passes over the batch until
+    about budget_s of CPU work (wall time x worker processes) is spent."""
+    op = OraclePool(w)
+    try:
+        B = len(op.batch.seq_lens)
+        all_heads = list(range(w.num_q_heads))
+        units = [(b, all_heads) for b in range(B)]
+        passes, secs = 0, 0.0
+        while passes == 0 or secs * op.cores < budget_s:
+            secs += op.run(units)
+            passes += 1
+        kvb = passes * kv_bytes(op.batch.seq_lens, w)
+        return {"value": round(kvb / secs / 1e9, 4), "unit": "GB/s", "cores": op.cores,
+                "kind": "oracle",
+                "sample": f"fp64 oracle, {passes} full pass(es) over the {B} sequences x "
+                          f"{w.num_q_heads} query heads of the {w.name} workload, {secs:.2f} s "
+                          f"wall on {op.cores} single-threaded worker processes",
+                "tokens_per_s": round(passes * B / secs, 3)}
+    finally:
+        op.close()
+
+
+def run_reference(args, dist_info):
+    rank, world, _ = dist_info
+    if rank != 0:
+        return None
+    w = workload(args.workload, args.block_size)
+    op = OraclePool(w)
+    try:
+        B = len(op.batch.seq_lens)
+        G = w.group
+        # unit = one (sequence, KV head): its G query heads
+        units = [(b, list(range(h * G, (h + 1) * G))) for b in range(B)
+                 for h in range(w.num_kv_heads)]
+        probe = units[:op.cores]
+        t = op.run(probe)
+        per_unit = t / len(probe)
+        total_steps = args.steps + args.warmup
+        budget = args.cpu_budget * 8          # whole reference run: a few minutes at most
+        n = max(1, min(len(units), int(budget / total_steps / max(per_unit, 1e-9))))
+        sample = units[:n]
+        for _ in range(args.warmup):
+            op.run(sample)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            op.run(sample)
+        secs = time.perf_counter() - t0
+        kvb = op.unit_bytes(sample) * args.steps
+        value = kvb / secs / 1e9
+        line = {
+            "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) q/K/V; block ids a seeded permutation)",
+            "config": {"workload": w.name, "num_seqs": B, "num_q_heads": w.num_q_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                       "block_size": w.block_size},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": op.cores,
+                             "kind": "oracle",
+                             "sample": f"each step: {n} (sequence, KV head) units of "
+                                       f"{len(units)} of the {w.name} workload, fp64 oracle"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        return line
+    finally:
+        op.close()
+
+
+# ----------------------------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "native":
+        import torch
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    return rank, world, local
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="llama3_8b",
+                    choices=["llama3_8b", "long_context", "ragged", "tiny"])
+    ap.add_argument("--block-size", type=int, default=None)
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    dist_info = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, dist_info)
+    else:
+        res = run_native(args, dist_info)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if dist_info[1] > 1 and args.impl == "native":
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+/*
+ * libpagedattn — PagedAttention decode on GB300 (sm_103a), C ABI.
+ *
+ * The KV cache of every sequence lives in fixed-size physical blocks of one
+ * preallocated pool; a per-sequence block table maps logical block i to a
+ * physical block id ("PagedAttention" glossary entry, block tables; "10 — Paged
+ * Attention" tutorial, §1 "What is it?").  This library provides the three
+ * device operations of a decode step over such a pool:
+ *
+ *   pa_decode             attention of one query token per sequence over its
+ *                         paged keys/values, the gather fused into the math
+ *                         (tutorial §5 "The kernel side"; glossary entry, the
+ *                         kernel duties: read the table, gather, handle a
+ *                         partly filled last block);
+ *   pa_reshape_and_cache  store new tokens' keys/values in pool slots;
+ *   pa_copy_blocks        whole-block copies for copy-on-write (tutorial §5
+ *                         "Copy-on-write sharing"; subroutine-cs article §3);
+ *
+ * plus pa_decode_slots (the slot of each sequence's newest token, the
+ * tutorial's PhysicalIndex, §4) and a host-side block manager (pa_bm_*,
+ * tutorial §4 "Tiny example": allocate / free / fork / append).
+ *
+ * Conventions for every device call
+ *   - All tensors are dense, row-major, in device memory owned by the caller.
+ *     The library allocates no device memory and keeps no global device state;
+ *     pa_decode's scratch space is a caller-provided workspace.
+ *   - K and V pools share one layout: [num_blocks, block_size, num_kv_heads,
+ *     head_dim], so slot s (= block * block_size + row) of the pool is one
+ *     contiguous row of num_kv_heads * head_dim elements.
+ *   - Element type is fp16 or bf16 (pa_dtype); q, out, key, value and the
+ *     pools of one call share it.  Index arrays are int32.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  Host-side
+ *     argument checks run before any launch and return an error code without
+ *     launching; a launch failure returns PA_ERR_CUDA.  No call aborts.
+ *   - status_dev (nullable): an int32 in device memory.  When non-NULL the call
+ *     runs in checked mode: invalid device-side data (a block id outside
+ *     [0, num_blocks), a slot outside the pool, a sequence longer than its
+ *     table) is reported by storing the error code there, and the offending
+ *     access is skipped.  The caller zeroes it beforehand.  With NULL such data
+ *     is a caller error (reads through the tensor-map path stay inside the
+ *     pool; other accesses are unchecked).
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* null pointer, bad shape or size            */
+  PA_ERR_UNSUPPORTED = 2,   /* dtype / head_dim / block_size not built     */
+  PA_ERR_WORKSPACE = 3,     /* workspace missing or too small              */
+  PA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed        */
+  PA_ERR_BAD_BLOCK_ID = 5,  /* checked mode: bad block id / slot / length  */
+  PA_ERR_OUT_OF_BLOCKS = 6, /* block manager: free pool too small          */
+  PA_ERR_BLOCK_STATE = 7    /* block manager: unreferenced block freed or
+                               forked, unknown sequence                    */
+} pa_status;
+
+typedef enum pa_dtype { PA_FLOAT16 = 0, PA_BFLOAT16 = 1 } pa_dtype;
+
+/* Human-readable name of a status code (static string). */
+const char* pa_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int pa_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Workspace bytes pa_decode needs for a batch of num_seqs sequences no longer
+ * than max_seq_len tokens.  partition_tokens: 0 selects the default (512).
+ * Returns 0 for invalid arguments.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                 int max_seq_len, int partition_tokens);
+
+/*
+ * out[b, hq, :] = sum_t softmax_t(scale * q[b, hq, :] . K[slot_t, hq / G, :])
+ *                       * V[slot_t, hq / G, :]
+ * over t < seq_lens[b], slot_t = block_tables[b][t / block_size] * block_size
+ * + t % block_size, G = num_q_heads / num_kv_heads (query head hq reads KV
+ * head hq / G).  This is exact softmax attention; the pool indirection only
+ * decides where rows are read from (glossary entry, the kernel duties; tutorial
+ * §4 PhysicalIndex and §5 "The kernel side").
+ *
+ * out, q        [num_seqs, num_q_heads, head_dim]          dtype
+ * k_pool/v_pool [num_blocks, block_size, num_kv_heads, head_dim]   dtype
+ * block_tables  [num_seqs, max_blocks] int32; entries past
+ *               ceil(seq_len / block_size) are never read
+ * seq_lens      [num_seqs] int32, 0 <= seq_len <= max_seq_len; a sequence of
+ *               length 0 gets a zero output row
+ * max_seq_len   host-side upper bound on seq_lens (sizes the launch without a
+ *               device-to-host read); a longer or negative seq_len is clamped
+ *               to [0, max_seq_len] (and reported in checked mode)
+ * scale         softmax scale applied to q.k (fp32)
+ * partition_tokens  tokens per split-K partition (multiple of 128 and of
+ *               block_size); 0 = default 512.  Sequences longer than one
+ *               partition are processed as independent partitions whose
+ *               partial (max, sum, accumulator) are merged by a second pass.
+ * workspace     device scratch of at least pa_decode_workspace_bytes(...),
+ *               256-byte aligned; contents need not be initialised; it may
+ *               not be shared by calls that overlap on the GPU.
+ * Supported: dtype fp16/bf16, head_dim 64 or 128, block_size 8/16/32/64,
+ * num_q_heads a multiple of num_kv_heads.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                    const int32_t* block_tables, const int32_t* seq_lens,
+                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                    int block_size, int max_blocks, int num_blocks, int max_seq_len,
+                    float scale, int dtype, int partition_tokens,
+                    void* workspace, size_t workspace_bytes,
+                    int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Cache writes                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For i < num_tokens with slot = slot_mapping[i] >= 0:
+ *   k_pool[slot / block_size][slot % block_size][:, :] = key[i][:, :]
+ *   v_pool[...same...]                                   = value[i][:, :]
+ * i.e. token i's [num_kv_heads, head_dim] rows land in pool slot `slot`, the
+ * tutorial's PhysicalIndex of the token's position (§4).  Negative slots mark
+ * padding and are skipped.  Exact bit copies.
+ *
+ * key/value     [num_tokens, num_kv_heads, head_dim] with token stride
+ *               kv_token_stride elements (0 = num_kv_heads * head_dim); rows
+ *               must be 16-byte aligned.
+ * Two tokens mapped to the same slot in one call is a caller error.
+ */
+pa_status pa_reshape_and_cache(void* k_pool, void* v_pool, const void* key, const void* value,
+                               const int32_t* slot_mapping, int num_tokens,
+                               int64_t kv_token_stride, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, int dtype,
+                               int32_t* status_dev, cudaStream_t stream);
+
+/*
+ * Copy-on-write clone: for each pair (src, dst) = (block_pairs[2i],
+ * block_pairs[2i+1]), i < num_pairs, copy every slot of block src to block dst,
+ * in both pools (tutorial §5 "Copy-on-write sharing": copy first, then write).
+ * Pairs are copied concurrently: a dst that is also a src, or a dst that
+ * appears twice, in one call is a caller error.  Exact bit copies.
+ */
+pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* block_pairs, int num_pairs,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         int dtype, int32_t* status_dev, cudaStream_t stream);
+
+/*
+ * slot_mapping[b] = slot of token seq_lens[b] - 1 of sequence b (its newest
+ * token), block_tables[b][(L-1) / block_size] * block_size + (L-1) % block_size,
+ * or -1 when seq_lens[b] == 0 (tutorial §4 PhysicalIndex).  Feeds
+ * pa_reshape_and_cache in a decode step.
+ */
+pa_status pa_decode_slots(int32_t* slot_mapping, const int32_t* block_tables,
+                          const int32_t* seq_lens, int num_seqs, int max_blocks,
+                          int block_size, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Host block manager                                                        */
+/* ------------------------------------------------------------------------ */
+/*
+ * Refcounted allocator of physical block ids (tutorial §4 "Tiny example"):
+ * a LIFO free stack; allocating n blocks hands out the top n entries in stack
+ * order with refcount 1, or fails leaving the state unchanged; freeing drops
+ * a refcount and returns the block to the stack at zero; forking raises the
+ * refcount of every block of a table.  Sequences (block table + length) grow
+ * one token at a time; a token that lands in a shared block triggers
+ * copy-on-write (new block, (old, new) pair reported for pa_copy_blocks,
+ * old refcount - 1).  Host memory only; not thread-safe per handle.
+ */
+typedef struct pa_block_manager pa_block_manager;
+
+/* initial_free_stack: NULL = ids num_blocks-1 .. 0 pushed in that order (id 0 on
+ * top); else a permutation of [0, num_blocks) listed bottom to top. */
+pa_status pa_bm_create(int num_blocks, int block_size, const int32_t* initial_free_stack,
+                       pa_block_manager** out);
+void pa_bm_destroy(pa_block_manager* bm);
+int pa_bm_num_free(const pa_block_manager* bm);
+/* Refcount of a block id (0 when free, -1 when out of range). */
+int pa_bm_refcount(const pa_block_manager* bm, int block_id);
+pa_status pa_bm_allocate(pa_block_manager* bm, int n, int32_t* out_ids);
+pa_status pa_bm_free(pa_block_manager* bm, const int32_t* ids, int n);
+pa_status pa_bm_fork(pa_block_manager* bm, const int32_t* ids, int n);
+
+/* Sequences are numbered by the manager; ids are never reused. */
+pa_status pa_bm_seq_create(pa_block_manager* bm, int prompt_len, int* seq_id);
+pa_status pa_bm_seq_fork(pa_block_manager* bm, int parent, int* child);
+pa_status pa_bm_seq_release(pa_block_manager* bm, int seq_id);
+/* Append one token.  *slot = its pool slot; (*cow_src, *cow_dst) = the block
+ * copy the caller must run before writing the token, or (-1, -1). */
+pa_status pa_bm_seq_append(pa_block_manager* bm, int seq_id, int32_t* slot,
+                           int32_t* cow_src, int32_t* cow_dst);
+int pa_bm_seq_len(const pa_block_manager* bm, int seq_id);
+int pa_bm_seq_num_blocks(const pa_block_manager* bm, int seq_id);
+/* Copy sequence tables into a [n, max_blocks] int32 array (padding with pad_id)
+ * and their lengths into seq_lens[n]; fails if a table is longer than max_blocks. */
+pa_status pa_bm_export(const pa_block_manager* bm, const int* seq_ids, int n, int max_blocks,
+                       int32_t pad_id, int32_t* block_tables, int32_t* seq_lens);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,221 @@
+"""PagedAttention decode for GB300 — thin Python binding over libpagedattn.
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels (or, for the block manager, its C++ host code).  Tensors are PyTorch
+tensors used as device buffers; the current CUDA stream is passed through.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+
+FLOAT16 = 0
+BFLOAT16 = 1
+_DTYPES = {torch.float16: FLOAT16, torch.bfloat16: BFLOAT16}
+
+PA_OK = 0
+DEFAULT_PARTITION_TOKENS = 512
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.load().pa_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != PA_OK:
+        raise PagedAttnError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libpagedattn must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}; use float16 or bfloat16") from None
+
+
+def lib() -> ctypes.CDLL:
+    return _lib.load()
+
+
+def pa_decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,
+                              max_seq_len: int, partition_tokens: int = 0) -> int:
+    return int(lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len,
+                                               partition_tokens))
+
+
+def alloc_workspace(num_seqs, num_q_heads, head_dim, max_seq_len, partition_tokens=0,
+                    device="cuda") -> torch.Tensor:
+    n = pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len, partition_tokens)
+    if n == 0:
+        raise ValueError("invalid workspace arguments")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def pa_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+              block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+              max_seq_len: Optional[int] = None, partition_tokens: int = 0,
+              workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
+    """Decode attention over a paged pool (see include/pagedattn.h, pa_decode).
+
+    q, out [B, Hq, D]; k_pool, v_pool [NB, bs, Hkv, D]; block_tables [B, MB] int32;
+    seq_lens [B] int32.  max_seq_len defaults to the table capacity MB * bs (no
+    device read); workspace is allocated when not given."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, Dk = k_pool.shape
+    MB = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = MB * bs
+    if workspace is None:
+        workspace = alloc_workspace(B, Hq, D, max_seq_len, partition_tokens, q.device)
+    st = lib().pa_decode(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens),
+        B, Hq, Hkv, D, bs, MB, NB, int(max_seq_len), float(scale), _dtype(q),
+        int(partition_tokens), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream(stream))
+    _check(st, "pa_decode")
+    return out
+
+
+def pa_reshape_and_cache(k_pool: torch.Tensor, v_pool: torch.Tensor, key: torch.Tensor,
+                         value: torch.Tensor, slot_mapping: torch.Tensor,
+                         status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Store new tokens' K/V ([T, Hkv, D]) at pool slots slot_mapping[T] (int32)."""
+    NB, bs, Hkv, D = k_pool.shape
+    T = key.shape[0]
+    st = lib().pa_reshape_and_cache(
+        _ptr(k_pool), _ptr(v_pool), _ptr(key), _ptr(value), _ptr(slot_mapping), T, 0,
+        Hkv, D, bs, NB, _dtype(k_pool), _ptr(status), _stream(stream))
+    _check(st, "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, block_pairs: torch.Tensor,
+                   status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Copy-on-write block clones; block_pairs [n, 2] int32 (src, dst)."""
+    NB, bs, Hkv, D = k_pool.shape
+    n = block_pairs.shape[0] if block_pairs.numel() else 0
+    st = lib().pa_copy_blocks(
+        _ptr(k_pool), _ptr(v_pool), _ptr(block_pairs) if n else None, n, Hkv, D, bs, NB,
+        _dtype(k_pool), _ptr(status), _stream(stream))
+    _check(st, "pa_copy_blocks")
+
+
+def pa_decode_slots(slot_mapping: torch.Tensor, block_tables: torch.Tensor,
+                    seq_lens: torch.Tensor, block_size: int, stream=None) -> torch.Tensor:
+    """slot_mapping[b] = pool slot of token seq_lens[b] - 1 (or -1 for empty)."""
+    B, MB = block_tables.shape
+    st = lib().pa_decode_slots(_ptr(slot_mapping), _ptr(block_tables), _ptr(seq_lens), B, MB,
+                               block_size, _stream(stream))
+    _check(st, "pa_decode_slots")
+    return slot_mapping
+
+
+class BlockManager:
+    """Host block manager of libpagedattn (pa_bm_*): allocate / free / fork and
+    sequences that append one token at a time with copy-on-write."""
+
+    def __init__(self, num_blocks: int, block_size: int,
+                 free_stack: Optional[Sequence[int]] = None):
+        self._lib = lib()
+        handle = ctypes.c_void_p()
+        arr = None
+        if free_stack is not None:
+            arr = (ctypes.c_int32 * num_blocks)(*[int(x) for x in free_stack])
+        _check(self._lib.pa_bm_create(num_blocks, block_size, arr, ctypes.byref(handle)),
+               "pa_bm_create")
+        self._h = handle
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.pa_bm_destroy(h)
+            self._h = None
+
+    @property
+    def num_free(self) -> int:
+        return self._lib.pa_bm_num_free(self._h)
+
+    def refcount(self, block: int) -> int:
+        return self._lib.pa_bm_refcount(self._h, block)
+
+    def allocate(self, n: int) -> list:
+        out = (ctypes.c_int32 * max(n, 1))()
+        _check(self._lib.pa_bm_allocate(self._h, n, out), "pa_bm_allocate")
+        return list(out)[:n]
+
+    def free(self, ids: Sequence[int]) -> None:
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(self._lib.pa_bm_free(self._h, arr, len(ids)), "pa_bm_free")
+
+    def fork_blocks(self, ids: Sequence[int]) -> None:
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(self._lib.pa_bm_fork(self._h, arr, len(ids)), "pa_bm_fork")
+
+    def new_sequence(self, prompt_len: int) -> int:
+        sid = ctypes.c_int()
+        _check(self._lib.pa_bm_seq_create(self._h, prompt_len, ctypes.byref(sid)),
+               "pa_bm_seq_create")
+        return sid.value
+
+    def fork(self, seq: int) -> int:
+        sid = ctypes.c_int()
+        _check(self._lib.pa_bm_seq_fork(self._h, seq, ctypes.byref(sid)), "pa_bm_seq_fork")
+        return sid.value
+
+    def release(self, seq: int) -> None:
+        _check(self._lib.pa_bm_seq_release(self._h, seq), "pa_bm_seq_release")
+
+    def append(self, seq: int):
+        """Returns (slot, (src, dst) copy-on-write pair or None)."""
+        slot, src, dst = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.pa_bm_seq_append(self._h, seq, ctypes.byref(slot), ctypes.byref(src),
+                                          ctypes.byref(dst)), "pa_bm_seq_append")
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def seq_len(self, seq: int) -> int:
+        return self._lib.pa_bm_seq_len(self._h, seq)
+
+    def seq_num_blocks(self, seq: int) -> int:
+        return self._lib.pa_bm_seq_num_blocks(self._h, seq)
+
+    def export(self, seqs: Sequence[int], max_blocks: int, pad_id: int):
+        """(block_tables [n, max_blocks] int32, seq_lens [n] int32) as CPU tensors."""
+        n = len(seqs)
+        ids = (ctypes.c_int * max(n, 1))(*seqs)
+        tables = torch.empty((n, max_blocks), dtype=torch.int32)
+        lens = torch.empty((n,), dtype=torch.int32)
+        _check(self._lib.pa_bm_export(self._h, ids, n, max_blocks, pad_id, tables.data_ptr(),
+                                      lens.data_ptr()), "pa_bm_export")
+        return tables, lens
+
+
+__all__ = [
+    "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_workspace_bytes",
+    "alloc_workspace", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_slots",
+    "BlockManager", "lib",
+]

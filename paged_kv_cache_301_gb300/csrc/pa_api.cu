@@ -1,0 +1,110 @@
+// C ABI of pa_decode: argument checks, workspace carve-up, kernel choice.
+#include <math.h>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WorkspaceLayout workspace_layout(int B, int Hq, int D, int P) {
+  const size_t rows = (size_t)B * Hq * P;
+  WorkspaceLayout w;
+  w.m_off = 0;
+  w.l_off = align256(rows * sizeof(float));
+  w.acc_off = w.l_off + align256(rows * sizeof(float));
+  w.total = w.acc_off + align256(rows * D * sizeof(float));
+  if (w.total == 0) w.total = 256;
+  return w;
+}
+
+static bool valid_partition(int pt) { return pt >= 128 && pt <= 1024 && pt % 128 == 0; }
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported dtype, head_dim or block_size";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_BAD_BLOCK_ID: return "invalid block id, slot or sequence length in device data";
+    case PA_ERR_OUT_OF_BLOCKS: return "out of KV blocks";
+    case PA_ERR_BLOCK_STATE: return "block or sequence in the wrong state";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int pa_version(void) { return 100; }
+
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                            int max_seq_len, int partition_tokens) {
+  const int pt = partition_tokens == 0 ? kDefaultPartitionTokens : partition_tokens;
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0 ||
+      !valid_partition(pt))
+    return 0;
+  const int P = max(1, num_partitions(max_seq_len, pt));
+  return workspace_layout(num_seqs, num_q_heads, head_dim, P).total;
+}
+
+extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, int max_blocks, int num_blocks, int max_seq_len,
+                               float scale, int dtype, int partition_tokens, void* workspace,
+                               size_t workspace_bytes, int32_t* status_dev,
+                               cudaStream_t stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks <= 0 ||
+      num_blocks <= 0 || max_seq_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+  if (!(head_dim == 64 || head_dim == 128)) return PA_ERR_UNSUPPORTED;
+  if (!(block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64))
+    return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_FLOAT16 && dtype != PA_BFLOAT16) return PA_ERR_UNSUPPORTED;
+  const int pt = partition_tokens == 0 ? kDefaultPartitionTokens : partition_tokens;
+  if (!valid_partition(pt) || pt % block_size) return PA_ERR_INVALID_ARG;
+  if ((long long)max_seq_len > (long long)max_blocks * block_size) return PA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
+  if ((((uintptr_t)out | (uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool) & 15u) != 0)
+    return PA_ERR_INVALID_ARG;
+  const int P = max(1, num_partitions(max_seq_len, pt));
+  const WorkspaceLayout wl = workspace_layout(num_seqs, num_q_heads, head_dim, P);
+  if (!workspace || workspace_bytes < wl.total || ((uintptr_t)workspace & 255u) != 0)
+    return PA_ERR_WORKSPACE;
+
+  DecodeParams p;
+  p.out = out;
+  p.q = q;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.B = num_seqs;
+  p.Hq = num_q_heads;
+  p.Hkv = num_kv_heads;
+  p.D = head_dim;
+  p.bs = block_size;
+  p.max_blocks = max_blocks;
+  p.num_blocks = num_blocks;
+  p.max_seq_len = max_seq_len;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.dtype = dtype;
+  p.PT = pt;
+  p.P = P;
+  char* ws = static_cast<char*>(workspace);
+  p.ws_m = reinterpret_cast<float*>(ws + wl.m_off);
+  p.ws_l = reinterpret_cast<float*>(ws + wl.l_off);
+  p.ws_acc = reinterpret_cast<float*>(ws + wl.acc_off);
+  p.status_dev = status_dev;
+
+  pa_status st = launch_decode_simt(p, stream);
+  if (st != PA_OK || P == 1) return st;
+  return launch_combine(p, stream);
+}

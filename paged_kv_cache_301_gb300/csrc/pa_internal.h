@@ -1,0 +1,39 @@
+// Internal launch interface shared by libpagedattn's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedattn.h"
+
+namespace pa {
+
+// Everything a decode launch needs, resolved on the host.
+struct DecodeParams {
+  void* out;
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  int B, Hq, Hkv, D, bs, max_blocks, num_blocks, max_seq_len;
+  float scale_log2;      // softmax scale * log2(e): scores are kept in base 2
+  int dtype;
+  int PT;                // tokens per split-K partition
+  int P;                 // partitions of the longest allowed sequence
+  float* ws_m;           // [B, Hq, P] running max (base 2) per partition
+  float* ws_l;           // [B, Hq, P] sum of exp2(s - m) per partition
+  float* ws_acc;         // [B, Hq, P, D] unnormalised partial outputs
+  int32_t* status_dev;   // nullable: checked mode
+};
+
+// Workspace carve-up; identical for every decode kernel.
+struct WorkspaceLayout {
+  size_t m_off, l_off, acc_off, total;
+};
+WorkspaceLayout workspace_layout(int B, int Hq, int D, int P);
+
+pa_status launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+pa_status launch_combine(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace pa

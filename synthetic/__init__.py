@@ -194,9 +194,16 @@ def token_kv_bits(w: Workload, num_tokens: int, sub: int) -> tuple:
     return normal_bits(g, shape, w.dtype), normal_bits(g, shape, w.dtype)
 
 
-def pool_fill_bits(w: Workload, num_blocks: int, sub: int = 0) -> tuple:
+def pool_fill_bits(w: Workload, num_blocks: int, sub: int = 0, chunk_blocks: int = 4096) -> tuple:
     """A whole pool of random K and V bits, [NB, bs, Hkv, D] each (used where the
-    values of every slot are random data rather than specific tokens)."""
+    values of every slot are random data rather than specific tokens).  Drawn in
+    chunks of blocks to bound host memory."""
     g = rng(w, "values", 10_000 + sub)
     shape = (num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
-    return normal_bits(g, shape, w.dtype), normal_bits(g, shape, w.dtype)
+    k = np.empty(shape, dtype=np.uint16)
+    v = np.empty(shape, dtype=np.uint16)
+    for lo in range(0, num_blocks, chunk_blocks):
+        hi = min(num_blocks, lo + chunk_blocks)
+        k[lo:hi] = normal_bits(g, (hi - lo,) + shape[1:], w.dtype)
+        v[lo:hi] = normal_bits(g, (hi - lo,) + shape[1:], w.dtype)
+    return k, v

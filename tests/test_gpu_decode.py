@@ -1,0 +1,218 @@
+"""GPU parity of pa_decode against the fp64 oracle, through the C ABI.
+
+Acceptance: |gpu - oracle| <= 2e-3 + 1e-2 |oracle| elementwise (fp32
+accumulation, fp16/bf16 storage; the output's own rounding is at most 2^-9
+relative for bf16, 2^-11 for fp16, well inside the relative term).  Closed forms
+whose exact result is representable are checked bit for bit."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic as syn
+from oracle import scenarios
+from oracle.attention import paged_decode_attention, storage_to_f64
+from oracle.brute import brute_decode_attention
+from tests.gpu_helpers import DeviceBatch, assert_close, i32, lib, to_dev, to_host_bits, widen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    return lib()
+
+
+def test_tiny_workload_matches_oracle_and_brute_force(pa):
+    batch = scenarios.fixed_batch(syn.TINY)
+    dev = DeviceBatch(batch)
+    got = widen(dev.decode(pa))
+    ref = scenarios.decode_f64(batch)
+    assert_close(got, ref, "tiny")
+    dt = batch.dtype
+    brute = np.array(brute_decode_attention(
+        storage_to_f64(batch.q, dt).tolist(), storage_to_f64(batch.k_pool, dt).tolist(),
+        storage_to_f64(batch.v_pool, dt).tolist(), batch.block_tables.tolist(),
+        batch.seq_lens.tolist(), float(np.float32(batch.scale)), batch.block_size))
+    assert_close(got, brute, "tiny vs brute force")
+
+
+def test_llama3_8b_workload_all_rows(pa):
+    batch = scenarios.fixed_batch(syn.LLAMA3_8B)
+    dev = DeviceBatch(batch)
+    got = widen(dev.decode(pa))
+    assert_close(got, scenarios.decode_f64(batch), "llama3_8b")
+
+
+@pytest.fixture(scope="module")
+def long_context():
+    return scenarios.fixed_batch(syn.LONG_CONTEXT, fill_all=True)
+
+
+def test_long_context_full_size_sampled_rows(pa, long_context):
+    """Full-size long-context batch in the benchmark's launch configuration
+    (split-K 512 + combine); sampled rows against the oracle, all rows finite."""
+    batch = long_context
+    dev = DeviceBatch(batch)
+    out = dev.decode(pa, partition_tokens=512)
+    got = widen(out)
+    assert np.isfinite(got).all()
+    seqs = [0, 3, 6]
+    heads = [0, 7, 8, 33, 63]
+    ref = scenarios.decode_f64(batch, sequences=seqs, heads=heads)
+    for b in seqs:
+        assert_close(got[b, heads], ref[b, heads], f"long_context b={b}")
+
+
+def _small(name, **kw):
+    base = syn.WORKLOADS[name] if name in syn.WORKLOADS else syn.LLAMA3_8B
+    return dataclasses.replace(base, **kw)
+
+
+@pytest.mark.parametrize("dtype", [syn.FLOAT16, syn.BFLOAT16])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+def test_shapes_with_ragged_tails(pa, dtype, head_dim, bs):
+    lens = [1, 2, bs - 1, bs, bs + 1, 127, 128, 129, 511, 512, 513, 1000, 1024, 1025, 1537]
+    w = _small("llama3_8b", num_seqs=len(lens), dtype=dtype, head_dim=head_dim, block_size=bs,
+               seed=1000 + bs + head_dim + dtype, length_kind="fixed", lens=tuple(lens),
+               num_q_heads=8, num_kv_heads=2)
+    batch = scenarios.fixed_batch(w)
+    dev = DeviceBatch(batch)
+    got = widen(dev.decode(pa))
+    assert_close(got, scenarios.decode_f64(batch), f"dt={dtype} D={head_dim} bs={bs}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (32, 8), (64, 8), (32, 2), (24, 3),
+                                    (16, 1)])
+def test_query_groupings(pa, hq, hkv):
+    lens = [3, 70, 600, 1300]
+    w = _small("llama3_8b", num_seqs=4, num_q_heads=hq, num_kv_heads=hkv, length_kind="fixed",
+               lens=tuple(lens), seed=77 + hq + hkv)
+    batch = scenarios.fixed_batch(w)
+    got = widen(DeviceBatch(batch).decode(pa))
+    assert_close(got, scenarios.decode_f64(batch), f"Hq={hq} Hkv={hkv}")
+
+
+@pytest.mark.parametrize("pt", [128, 256, 512, 1024])
+def test_partition_sizes(pa, pt):
+    lens = [1, 127, 128, 129, 1024, 2049, 3000]
+    w = _small("llama3_8b", num_seqs=len(lens), length_kind="fixed", lens=tuple(lens), seed=5 + pt)
+    batch = scenarios.fixed_batch(w)
+    got = widen(DeviceBatch(batch).decode(pa, partition_tokens=pt))
+    assert_close(got, scenarios.decode_f64(batch), f"partition {pt}")
+
+
+def test_zero_length_sequences_give_zero_rows(pa):
+    w = _small("llama3_8b", num_seqs=4, length_kind="fixed", lens=(5, 1, 700, 3), seed=9)
+    batch = scenarios.fixed_batch(w)
+    dev = DeviceBatch(batch)
+    lens = batch.seq_lens.copy()
+    lens[1] = 0
+    lens[3] = 0
+    out = dev.decode(pa, lens=i32(lens), max_seq_len=int(lens.max()))
+    got = widen(out)
+    assert not got[1].any() and not got[3].any()
+    ref = paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.block_tables, lens,
+                                 batch.scale, dtype=batch.dtype)
+    assert_close(got, ref, "zero-length rows")
+
+
+def test_length_one_is_exact(pa):
+    w = _small("llama3_8b", num_seqs=16, length_kind="fixed", lens=(1,) * 16, seed=11)
+    batch = scenarios.fixed_batch(w)
+    out = to_host_bits(DeviceBatch(batch).decode(pa))
+    G = w.group
+    for b in range(16):
+        blk = batch.block_tables[b, 0]
+        for hq in range(w.num_q_heads):
+            assert np.array_equal(out[b, hq], batch.v_pool[blk, 0, hq // G])
+
+
+def test_constant_values_and_equal_keys(pa):
+    w = _small("llama3_8b", num_seqs=6, length_kind="fixed", lens=(9, 100, 513, 1024, 2000, 1),
+               seed=12)
+    batch = scenarios.fixed_batch(w)
+    c = syn.fp32_to_storage_bits(np.float32(0.8125), w.dtype)
+    batch.v_pool[...] = c
+    out = widen(DeviceBatch(batch).decode(pa))
+    assert np.all(out == 0.8125)
+    batch = scenarios.fixed_batch(w)
+    batch.k_pool[...] = syn.fp32_to_storage_bits(np.float32(0.5), w.dtype)
+    got = widen(DeviceBatch(batch).decode(pa))
+    assert_close(got, scenarios.decode_f64(batch), "equal keys (mean of V)")
+
+
+def test_relabelled_blocks_give_identical_bits(pa):
+    """Permuting physical block ids (pool and tables together) leaves the output
+    bit-identical: no atomics, the reduction order depends on logical positions only."""
+    w = _small("llama3_8b", num_seqs=8, length_kind="fixed",
+               lens=(17, 300, 512, 777, 1500, 2048, 2600, 4096), seed=13)
+    batch = scenarios.fixed_batch(w)
+    out1 = to_host_bits(DeviceBatch(batch).decode(pa))
+    out1b = to_host_bits(DeviceBatch(batch).decode(pa))
+    assert np.array_equal(out1, out1b)
+    perm = np.random.default_rng(3).permutation(batch.num_blocks)
+    kp = np.empty_like(batch.k_pool)
+    vp = np.empty_like(batch.v_pool)
+    kp[perm] = batch.k_pool
+    vp[perm] = batch.v_pool
+    batch.k_pool, batch.v_pool = kp, vp
+    batch.block_tables = perm[batch.block_tables].astype(np.int32)
+    out2 = to_host_bits(DeviceBatch(batch).decode(pa))
+    assert np.array_equal(out1, out2)
+
+
+def test_forked_tables_give_identical_rows(pa):
+    w = _small("llama3_8b", num_seqs=4, length_kind="fixed", lens=(1000, 1000, 40, 40), seed=14)
+    batch = scenarios.fixed_batch(w)
+    batch.block_tables[1] = batch.block_tables[0]
+    batch.block_tables[3] = batch.block_tables[2]
+    batch.q[1] = batch.q[0]
+    batch.q[3] = batch.q[2]
+    out = to_host_bits(DeviceBatch(batch).decode(pa))
+    assert np.array_equal(out[0], out[1]) and np.array_equal(out[2], out[3])
+
+
+def test_checked_mode_reports_bad_block_ids(pa):
+    w = _small("llama3_8b", num_seqs=3, length_kind="fixed", lens=(40, 600, 33), seed=15)
+    batch = scenarios.fixed_batch(w)
+    dev = DeviceBatch(batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev.decode(pa, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    tables = batch.block_tables.copy()
+    tables[1, 3] = batch.num_blocks + 5          # outside the pool
+    tables[2, 0] = -2
+    dev.decode(pa, tables=i32(tables), max_seq_len=600, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
+    assert dev.guards_intact()
+
+
+def test_too_long_sequence_is_reported_in_checked_mode(pa):
+    w = _small("llama3_8b", num_seqs=2, length_kind="fixed", lens=(40, 60), seed=16)
+    batch = scenarios.fixed_batch(w)
+    dev = DeviceBatch(batch)
+    lens = batch.seq_lens.copy()
+    lens[0] = batch.block_tables.shape[1] * w.block_size + 7
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = dev.decode(pa, lens=i32(lens), max_seq_len=batch.block_tables.shape[1] * w.block_size,
+                     status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
+    assert np.isfinite(widen(out)[1]).all()
+
+
+def test_bad_arguments_raise(pa):
+    batch = scenarios.fixed_batch(syn.TINY)
+    dev = DeviceBatch(batch)
+    with pytest.raises(pa.PagedAttnError):
+        pa.pa_decode(torch.empty_like(dev.q), dev.q, dev.k_pool, dev.v_pool, dev.tables,
+                     dev.lens, 0.125, max_seq_len=10_000)
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PagedAttnError):
+        pa.pa_decode(torch.empty_like(dev.q), dev.q, dev.k_pool, dev.v_pool, dev.tables,
+                     dev.lens, 0.125, max_seq_len=64, workspace=ws)
