@@ -65,7 +65,7 @@ def test_reshape_and_cache_out_of_range_slot_reported(pa):
 @pytest.mark.parametrize("bs", [8, 16, 32, 64])
 def test_copy_blocks_bit_exact(pa, bs):
     w = syn.LLAMA3_8B.__class__(**{**syn.LLAMA3_8B.__dict__, "block_size": bs,
-                                   "length_kind": "fixed", "lens": (300, 70), "num_seqs": 2})
+                                   "length_kind": "fixed", "lens": (900, 700), "num_seqs": 2})
     batch = scenarios.fixed_batch(w)
     batch.k_pool, batch.v_pool = syn.pool_fill_bits(w, batch.num_blocks, sub=bs)
     dev = DeviceBatch(batch)
