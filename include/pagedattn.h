@@ -120,6 +120,44 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
                     void* workspace, size_t workspace_bytes,
                     int32_t* status_dev, cudaStream_t stream);
 
+/*
+ * pa_decode for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this is a deployment convenience of this library.
+ *
+ * pa_decode needs a scratch workspace for its split-K partials, normally
+ * allocated by the caller.  Some callers cannot allocate when they call: code
+ * recorded into a CUDA graph where allocation is not permitted, plug-ins that
+ * only receive device pointers from a host application that owns every
+ * allocation, or latency-critical loops that must stay off the allocator.
+ * This entry point has the arguments of pa_decode minus the workspace and
+ * takes its scratch from a fixed array of PA_DECODE_NOALLOC_SCRATCH_BYTES
+ * (32 MiB) that is part of the library's device image: every device that
+ * loads the library holds it until the process exits.  It calls no
+ * allocating routine.
+ *
+ *  - Limit: a batch whose pa_decode_workspace_bytes(...) exceeds
+ *    PA_DECODE_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE before
+ *    any device work (e.g. 64 sequences x 32 query heads up to 4096 tokens
+ *    need about 8.1 MiB; 8 x 64 heads up to 128K tokens need about 65 MiB and
+ *    are rejected).  Other errors are those of pa_decode.
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current; this may load the module).
+ *    Make that first call before any stream capture.  The current device must
+ *    be the device of the buffers and of `stream`.
+ *  - Sharing: all calls share the one array, which keeps the last call's
+ *    contents; nothing in it needs to start at zero.  Calls that overlap on the
+ *    GPU (different streams, or different host threads without ordering) race
+ *    on it and give wrong results: serialise them.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks, int num_blocks, int max_seq_len,
+                            float scale, int dtype, int partition_tokens,
+                            int32_t* status_dev, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Cache writes                                                              */
 /* ------------------------------------------------------------------------ */

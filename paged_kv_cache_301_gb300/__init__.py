@@ -100,6 +100,28 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: 
     return out
 
 
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                      v_pool: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                      scale: float, max_seq_len: int, partition_tokens: int = 0,
+                      status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pa_decode without a caller workspace, for callers that cannot allocate
+    device memory when they call (see include/pagedattn.h, pa_decode_noalloc):
+    the split-K scratch is a fixed 32 MiB array inside the library, shared by
+    all calls, so calls must not overlap on the GPU."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, Dk = k_pool.shape
+    MB = block_tables.shape[1]
+    st = lib().pa_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens),
+        B, Hq, Hkv, D, bs, MB, NB, int(max_seq_len), float(scale), _dtype(q),
+        int(partition_tokens), _ptr(status), _stream(stream))
+    _check(st, "pa_decode_noalloc")
+    return out
+
+
 def pa_reshape_and_cache(k_pool: torch.Tensor, v_pool: torch.Tensor, key: torch.Tensor,
                          value: torch.Tensor, slot_mapping: torch.Tensor,
                          status: Optional[torch.Tensor] = None, stream=None) -> None:
@@ -216,6 +238,7 @@ class BlockManager:
 
 __all__ = [
     "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_workspace_bytes",
+    "pa_decode_noalloc",
     "alloc_workspace", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_slots",
     "BlockManager", "lib",
 ]

@@ -25,6 +25,7 @@ SOURCES = [
     "pa_cache.cu",
     "pa_decode_simt.cu",
     "pa_block_manager.cpp",
+    "pa_decode_noalloc.cu",
 ]
 HEADERS = [
     os.path.join(ROOT, "include", "pagedattn.h"),
