@@ -171,10 +171,17 @@ def recorded_traffic(workload_name: str):
     return None
 
 
+def decode_kernel_for(w, kernel: str) -> str:
+    """Which decode kernel runs: the tensor-core kernel serves head_dim 128."""
+    if kernel == "auto":
+        return "tc" if w.head_dim == 128 else "simt"
+    return kernel
+
+
 class NativeStep:
     """Device state of one replica: pool, tables, inputs; run() = one step."""
 
-    def __init__(self, pa, torch, w, dev, partition_tokens: int):
+    def __init__(self, pa, torch, w, dev, partition_tokens: int, kernel: str):
         self.pa, self.torch, self.w, self.dev = pa, torch, w, dev
         bs = w.block_size
         lens = syn.seq_lens(w)
@@ -211,7 +218,10 @@ class NativeStep:
         self.ws = pa.alloc_workspace(B, w.num_q_heads, w.head_dim, self.max_seq_len,
                                      partition_tokens, dev)
         P = -(-self.max_seq_len // (partition_tokens or 512))
-        self.launches_per_step = 3 + (1 if P > 1 else 0)
+        # decode_slots + reshape_and_cache + decode (+ plan on the tensor-core
+        # path) + combine when a sequence spans several partitions
+        self.kernel = decode_kernel_for(w, kernel)
+        self.launches_per_step = 3 + (1 if self.kernel == "tc" else 0) + (1 if P > 1 else 0)
         # pinned host copies for the end-to-end measurement
         self.h_q = self.q.cpu().pin_memory()
         self.h_key = self.key.cpu().pin_memory()
@@ -262,7 +272,8 @@ def run_native(args, dist_info):
     if rank == 0 and not args.no_cpu_baseline:
         # before the first GPU call: the oracle's pool is a spawn pool anyway
         cpu_baseline = cpu_oracle_baseline(w, budget_s=args.cpu_budget)
-    step = NativeStep(pa, torch, w, dev, args.partition_tokens)
+    pa.set_decode_path(args.kernel)
+    step = NativeStep(pa, torch, w, dev, args.partition_tokens, args.kernel)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -350,6 +361,8 @@ def run_native(args, dist_info):
             "l2": f"inputs larger than L2: {kvb / 2**20:.0f} MiB of K/V read per step vs "
                   f"{L2_BYTES / 2**20:.0f} MiB L2; no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "decode_kernel": {"tc": "tcgen05 + TMA (decode_tc_kernel)",
+                              "simt": "CUDA cores (decode_simt_kernel)"}[step.kernel],
         },
         "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
         "kv_frac_of_peak": round(value / world / peak, 4),
@@ -363,7 +376,8 @@ def run_native(args, dist_info):
         },
         "gpu_launches": step.launches_per_step * args.steps,
         "roofline": {
-            "kernel": "pa_decode (split-K main + combine)",
+            "kernel": "pa_decode (plan + split-K main + combine)" if step.kernel == "tc"
+                      else "pa_decode (split-K main + combine)",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -549,6 +563,7 @@ def main():
                     choices=["llama3_8b", "long_context", "ragged", "tiny"])
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()

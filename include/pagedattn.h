@@ -59,8 +59,10 @@ typedef enum pa_status {
   PA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed        */
   PA_ERR_BAD_BLOCK_ID = 5,  /* checked mode: bad block id / slot / length  */
   PA_ERR_OUT_OF_BLOCKS = 6, /* block manager: free pool too small          */
-  PA_ERR_BLOCK_STATE = 7    /* block manager: unreferenced block freed or
+  PA_ERR_BLOCK_STATE = 7,   /* block manager: unreferenced block freed or
                                forked, unknown sequence                    */
+  PA_ERR_TIMEOUT = 8        /* a kernel's bounded internal wait expired and
+                               it stopped early (reported via status_dev)  */
 } pa_status;
 
 typedef enum pa_dtype { PA_FLOAT16 = 0, PA_BFLOAT16 = 1 } pa_dtype;
@@ -119,6 +121,19 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
                     float scale, int dtype, int partition_tokens,
                     void* workspace, size_t workspace_bytes,
                     int32_t* status_dev, cudaStream_t stream);
+
+/*
+ * Kernel selection for pa_decode / pa_decode_noalloc (process-wide setting):
+ *   PA_DECODE_AUTO   tensor-core kernel (tcgen05 + TMA) when head_dim is 128,
+ *                    else the CUDA-core kernel (default);
+ *   PA_DECODE_SIMT   always the CUDA-core kernel;
+ *   PA_DECODE_TC     the tensor-core kernel; calls it cannot serve return
+ *                    PA_ERR_UNSUPPORTED.
+ * Returns PA_ERR_INVALID_ARG for an unknown value.  Not synchronised with
+ * calls in flight on other host threads.
+ */
+typedef enum pa_decode_path { PA_DECODE_AUTO = 0, PA_DECODE_SIMT = 1, PA_DECODE_TC = 2 } pa_decode_path;
+pa_status pa_set_decode_path(int path);
 
 /*
  * pa_decode for callers that cannot allocate device memory.  The pages have no

@@ -122,6 +122,15 @@ def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     return out
 
 
+DECODE_PATHS = {"auto": 0, "simt": 1, "tc": 2}
+
+
+def set_decode_path(name: str) -> None:
+    """Select the decode kernel process-wide: "auto" (tensor cores for head_dim
+    128, else CUDA cores), "simt" (CUDA cores) or "tc" (tensor cores only)."""
+    _check(lib().pa_set_decode_path(DECODE_PATHS[name]), "pa_set_decode_path")
+
+
 def pa_reshape_and_cache(k_pool: torch.Tensor, v_pool: torch.Tensor, key: torch.Tensor,
                          value: torch.Tensor, slot_mapping: torch.Tensor,
                          status: Optional[torch.Tensor] = None, stream=None) -> None:
@@ -238,7 +247,7 @@ class BlockManager:
 
 __all__ = [
     "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_workspace_bytes",
-    "pa_decode_noalloc",
+    "pa_decode_noalloc", "set_decode_path",
     "alloc_workspace", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_slots",
     "BlockManager", "lib",
 ]

@@ -33,6 +33,7 @@ SIGNATURES = {
                                      c_void_p]),
     "pa_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_void_p, c_void_p]),
+    "pa_set_decode_path": (c_int, [c_int]),
     "pa_decode_slots": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p]),
     "pa_bm_create": (c_int, [c_int, c_int, c_void_p, ctypes.POINTER(c_void_p)]),
     "pa_bm_destroy": (None, [c_void_p]),

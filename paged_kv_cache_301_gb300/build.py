@@ -26,6 +26,7 @@ SOURCES = [
     "pa_decode_simt.cu",
     "pa_block_manager.cpp",
     "pa_decode_noalloc.cu",
+    "pa_decode_tc.cu",
 ]
 HEADERS = [
     os.path.join(ROOT, "include", "pagedattn.h"),

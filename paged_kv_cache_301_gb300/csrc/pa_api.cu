@@ -11,13 +11,16 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 WorkspaceLayout workspace_layout(int B, int Hq, int D, int P) {
   const size_t rows = (size_t)B * Hq * P;
   WorkspaceLayout w;
-  w.m_off = 0;
-  w.l_off = align256(rows * sizeof(float));
+  w.queue_off = 0;                                   // work-queue counters
+  w.items_off = 256;                                 // (sequence, partition) pairs
+  w.m_off = w.items_off + align256((size_t)B * P * 2 * sizeof(int));
+  w.l_off = w.m_off + align256(rows * sizeof(float));
   w.acc_off = w.l_off + align256(rows * sizeof(float));
   w.total = w.acc_off + align256(rows * D * sizeof(float));
-  if (w.total == 0) w.total = 256;
   return w;
 }
+
+static int g_decode_path = PA_DECODE_AUTO;
 
 static bool valid_partition(int pt) { return pt >= 128 && pt <= 1024 && pt % 128 == 0; }
 
@@ -35,6 +38,7 @@ extern "C" const char* pa_status_string(int status) {
     case PA_ERR_BAD_BLOCK_ID: return "invalid block id, slot or sequence length in device data";
     case PA_ERR_OUT_OF_BLOCKS: return "out of KV blocks";
     case PA_ERR_BLOCK_STATE: return "block or sequence in the wrong state";
+    case PA_ERR_TIMEOUT: return "a kernel's bounded wait expired; results are incomplete";
     default: return "unknown status";
   }
 }
@@ -104,7 +108,23 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   p.ws_acc = reinterpret_cast<float*>(ws + wl.acc_off);
   p.status_dev = status_dev;
 
-  pa_status st = launch_decode_simt(p, stream);
+  const int path = g_decode_path;
+  const bool tc_ok = tc_supported(p);
+  pa_status st;
+  if (path == PA_DECODE_TC && !tc_ok) return PA_ERR_UNSUPPORTED;
+  if (path != PA_DECODE_SIMT && tc_ok) {
+    st = launch_decode_tc(p, reinterpret_cast<int2*>(ws + wl.items_off),
+                          reinterpret_cast<int*>(ws + wl.queue_off), stream);
+  } else {
+    st = launch_decode_simt(p, stream);
+  }
   if (st != PA_OK || P == 1) return st;
   return launch_combine(p, stream);
+}
+
+extern "C" pa_status pa_set_decode_path(int path) {
+  if (path != PA_DECODE_AUTO && path != PA_DECODE_SIMT && path != PA_DECODE_TC)
+    return PA_ERR_INVALID_ARG;
+  g_decode_path = path;
+  return PA_OK;
 }

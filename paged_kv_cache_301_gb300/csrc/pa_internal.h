@@ -29,11 +29,15 @@ struct DecodeParams {
 
 // Workspace carve-up; identical for every decode kernel.
 struct WorkspaceLayout {
-  size_t m_off, l_off, acc_off, total;
+  size_t queue_off, items_off, m_off, l_off, acc_off, total;
 };
 WorkspaceLayout workspace_layout(int B, int Hq, int D, int P);
 
 pa_status launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 pa_status launch_combine(const DecodeParams& p, cudaStream_t stream);
+
+// Tensor-core path (head_dim 128): plan kernel + persistent tcgen05 kernel.
+bool tc_supported(const DecodeParams& p);
+pa_status launch_decode_tc(const DecodeParams& p, int2* items, int* queue, cudaStream_t stream);
 
 }  // namespace pa

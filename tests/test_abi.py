@@ -80,7 +80,9 @@ def test_workspace_size(lib):
     n = lib.pa_decode_workspace_bytes(64, 32, 128, 4096, 0)
     P = 4096 // 512
     rows = 64 * 32 * P
-    assert n == 2 * ((rows * 4 + 255) // 256 * 256) + (rows * 128 * 4 + 255) // 256 * 256
+    a = lambda x: (x + 255) // 256 * 256
+    # queue counters, (sequence, partition) list, m, l, acc
+    assert n == 256 + a(64 * P * 8) + 2 * a(rows * 4) + a(rows * 128 * 4)
     assert lib.pa_decode_workspace_bytes(64, 32, 128, 4096, 100) == 0
     assert lib.pa_decode_workspace_bytes(-1, 32, 128, 4096, 0) == 0
 

@@ -13,9 +13,19 @@ from tests.gpu_helpers import DeviceBatch, assert_close, i32, lib, to_dev, to_ho
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def pa():
-    return lib()
+@pytest.fixture(scope="module", params=["simt", "tc"])
+def pa(request):
+    """Every test runs on the CUDA-core and on the tensor-core decode kernel."""
+    m = lib()
+    m.set_decode_path(request.param)
+    m.decode_path = request.param
+    yield m
+    m.set_decode_path("auto")
+
+
+def needs(pa, head_dim):
+    if pa.decode_path == "tc" and head_dim != 128:
+        pytest.skip("the tensor-core kernel serves head_dim 128")
 
 
 def _pools_equal(dev, k_ref, v_ref):

@@ -19,12 +19,23 @@ from tests.gpu_helpers import DeviceBatch, assert_close, i32, lib, to_dev, to_ho
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def pa():
-    return lib()
+@pytest.fixture(scope="module", params=["simt", "tc"])
+def pa(request):
+    """Every test runs on the CUDA-core and on the tensor-core decode kernel."""
+    m = lib()
+    m.set_decode_path(request.param)
+    m.decode_path = request.param
+    yield m
+    m.set_decode_path("auto")
+
+
+def needs(pa, head_dim):
+    if pa.decode_path == "tc" and head_dim != 128:
+        pytest.skip("the tensor-core kernel serves head_dim 128")
 
 
 def test_tiny_workload_matches_oracle_and_brute_force(pa):
+    needs(pa, syn.TINY.head_dim)
     batch = scenarios.fixed_batch(syn.TINY)
     dev = DeviceBatch(batch)
     got = widen(dev.decode(pa))
@@ -74,6 +85,7 @@ def _small(name, **kw):
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("bs", [8, 16, 32, 64])
 def test_shapes_with_ragged_tails(pa, dtype, head_dim, bs):
+    needs(pa, head_dim)
     lens = [1, 2, bs - 1, bs, bs + 1, 127, 128, 129, 511, 512, 513, 1000, 1024, 1025, 1537]
     w = _small("llama3_8b", num_seqs=len(lens), dtype=dtype, head_dim=head_dim, block_size=bs,
                seed=1000 + bs + head_dim + dtype, length_kind="fixed", lens=tuple(lens),
@@ -207,6 +219,7 @@ def test_too_long_sequence_is_reported_in_checked_mode(pa):
 
 
 def test_bad_arguments_raise(pa):
+    needs(pa, syn.TINY.head_dim)
     batch = scenarios.fixed_batch(syn.TINY)
     dev = DeviceBatch(batch)
     with pytest.raises(pa.PagedAttnError):
