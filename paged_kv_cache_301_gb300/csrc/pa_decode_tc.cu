@@ -591,6 +591,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p, int2* 
   const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
   int full = 0, part = 0;
   for (int b = b0; b < b1; ++b) {
+    const int raw = p.seq_lens[b];
+    if (raw < 0 || raw > p.max_seq_len) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
     const int L = clamp_seq_len(p, b);
     const int np = num_partitions(L, p.PT);
     const int f = (L % p.PT == 0) ? np : np - 1;
