@@ -123,16 +123,25 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
                     int32_t* status_dev, cudaStream_t stream);
 
 /*
- * Kernel selection for pa_decode / pa_decode_noalloc (process-wide setting):
- *   PA_DECODE_AUTO   tensor-core kernel (tcgen05 + TMA) when head_dim is 128,
- *                    else the CUDA-core kernel (default);
- *   PA_DECODE_SIMT   always the CUDA-core kernel;
- *   PA_DECODE_TC     the tensor-core kernel; calls it cannot serve return
- *                    PA_ERR_UNSUPPORTED.
- * Returns PA_ERR_INVALID_ARG for an unknown value.  Not synchronised with
- * calls in flight on other host threads.
+ * Kernel selection for pa_decode / pa_decode_noalloc (process-wide setting).
+ * Three decode kernels exist:
+ *   grouped tensor-core kernel (tcgen05 + TMA): each CTA reads whole blocks,
+ *     all KV heads at once, over an equal share of the batch's tokens;
+ *     head_dim 128, num_kv_heads 4 or 8, num_q_heads / num_kv_heads in {1,2,4,8};
+ *   per-head tensor-core kernel (tcgen05 + TMA): one KV head per work item;
+ *     head_dim 128, any grouping;
+ *   CUDA-core kernel: every supported shape.
+ *   PA_DECODE_AUTO     the first of the three that serves the call (default);
+ *   PA_DECODE_SIMT     always the CUDA-core kernel;
+ *   PA_DECODE_TC       a tensor-core kernel (grouped when it serves the call);
+ *   PA_DECODE_TC_HEAD  the per-head tensor-core kernel;
+ * a tensor-core setting returns PA_ERR_UNSUPPORTED for calls no tensor-core
+ * kernel serves.  Returns PA_ERR_INVALID_ARG for an unknown value.  Not
+ * synchronised with calls in flight on other host threads.
  */
-typedef enum pa_decode_path { PA_DECODE_AUTO = 0, PA_DECODE_SIMT = 1, PA_DECODE_TC = 2 } pa_decode_path;
+typedef enum pa_decode_path {
+  PA_DECODE_AUTO = 0, PA_DECODE_SIMT = 1, PA_DECODE_TC = 2, PA_DECODE_TC_HEAD = 3
+} pa_decode_path;
 pa_status pa_set_decode_path(int path);
 
 /*

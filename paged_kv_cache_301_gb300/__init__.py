@@ -122,12 +122,14 @@ def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     return out
 
 
-DECODE_PATHS = {"auto": 0, "simt": 1, "tc": 2}
+DECODE_PATHS = {"auto": 0, "simt": 1, "tc": 2, "tc_head": 3}
 
 
 def set_decode_path(name: str) -> None:
-    """Select the decode kernel process-wide: "auto" (tensor cores for head_dim
-    128, else CUDA cores), "simt" (CUDA cores) or "tc" (tensor cores only)."""
+    """Select the decode kernel process-wide: "auto" (the grouped tensor-core
+    kernel where it applies, else the per-head tensor-core kernel for head_dim
+    128, else CUDA cores), "simt" (CUDA cores), "tc" (a tensor-core kernel) or
+    "tc_head" (the per-head tensor-core kernel)."""
     _check(lib().pa_set_decode_path(DECODE_PATHS[name]), "pa_set_decode_path")
 
 

@@ -16,7 +16,8 @@ WorkspaceLayout workspace_layout(int B, int Hq, int D, int P) {
   w.m_off = w.items_off + align256((size_t)B * P * 2 * sizeof(int));
   w.l_off = w.m_off + align256(rows * sizeof(float));
   w.acc_off = w.l_off + align256(rows * sizeof(float));
-  w.total = w.acc_off + align256(rows * D * sizeof(float));
+  w.sk_off = w.acc_off + align256(rows * D * sizeof(float));
+  w.total = w.sk_off + sk_layout(B, Hq).total;
   return w;
 }
 
@@ -109,10 +110,12 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   p.status_dev = status_dev;
 
   const int path = g_decode_path;
-  const bool tc_ok = tc_supported(p);
+  const bool grouped = path != PA_DECODE_SIMT && path != PA_DECODE_TC_HEAD && tcg_supported(p);
+  if (grouped) return launch_decode_tcg(p, ws + wl.sk_off, stream);
+  const bool per_head = path != PA_DECODE_SIMT && tc_supported(p);
+  if ((path == PA_DECODE_TC || path == PA_DECODE_TC_HEAD) && !per_head) return PA_ERR_UNSUPPORTED;
   pa_status st;
-  if (path == PA_DECODE_TC && !tc_ok) return PA_ERR_UNSUPPORTED;
-  if (path != PA_DECODE_SIMT && tc_ok) {
+  if (per_head) {
     st = launch_decode_tc(p, reinterpret_cast<int2*>(ws + wl.items_off),
                           reinterpret_cast<int*>(ws + wl.queue_off), stream);
   } else {
@@ -123,7 +126,8 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
 }
 
 extern "C" pa_status pa_set_decode_path(int path) {
-  if (path != PA_DECODE_AUTO && path != PA_DECODE_SIMT && path != PA_DECODE_TC)
+  if (path != PA_DECODE_AUTO && path != PA_DECODE_SIMT && path != PA_DECODE_TC &&
+      path != PA_DECODE_TC_HEAD)
     return PA_ERR_INVALID_ARG;
   g_decode_path = path;
   return PA_OK;

@@ -715,18 +715,18 @@ pa_status launch_decode_tc(const DecodeParams& p, int2* items, int* queue,
   const cuuint32_t ones[3] = {1, 1, 1};
   if (enc(&tk, dt, 3, const_cast<void*>(p.k_pool), kv_dims, kv_strides, kv_box, ones,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return PA_ERR_INVALID_ARG;
   if (enc(&tv, dt, 3, const_cast<void*>(p.v_pool), kv_dims, kv_strides, kv_box, ones,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return PA_ERR_INVALID_ARG;
   const cuuint64_t q_dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.B * p.Hq};
   const cuuint64_t q_strides[1] = {(cuuint64_t)kD * 2};
   const cuuint32_t q_box[2] = {64, (cuuint32_t)kN};
   if (enc(&tq, dt, 2, const_cast<void*>(p.q), q_dims, q_strides, q_box, ones,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return PA_ERR_INVALID_ARG;
 
   TcParams tp;

@@ -1,0 +1,868 @@
+// pa_decode on the tensor cores, all KV heads of a block per CTA (grouped).
+//
+// A K/V block of the pool stores, per token, the rows of all Hkv heads next to
+// each other ([block_size][Hkv][D]), so one TMA copy with box
+// {64, Hkv, tokens} fetches a contiguous stretch of the block for all heads.
+// Per-head copies fetch 128-byte pieces 2 KB apart, which measured ~30% slower
+// on GB300 than whole-block copies.  This kernel therefore gives each CTA all
+// heads of a token range:
+//
+//   tile      = 128 rows = TT = 128 / Hkv tokens x Hkv heads, row = token * Hkv + head
+//   S         = K_tile[128 x 128] . Q^T[128 x N]       N = Hq rounded up to 16
+//   softmax   row (t, h) keeps the G columns of its own query heads h*G .. h*G+G-1
+//   P'        [128 rows x N], block diagonal: P'[(t,h), hq] = p(t, hq) when hq / G == h
+//   O^T       [128 x N] += V_tile^T . P'                (V read MN-major from the tile)
+// so every query head meets only the rows of its own KV head ("10 — Paged
+// Attention" tutorial, §5 "The kernel side": gather through the table; the head
+// mapping hq -> hq / G is this library's reading of grouped-query attention).
+// P' is stored as two storage-type terms (hi + lo, ~16 significant bits).
+//
+// Work split (stream-K): the batch is a sequence of token tiles, each sequence
+// padded to whole tiles; CTA c of the persistent grid takes the tiles
+// [c*T/grid, (c+1)*T/grid).  A sequence that lies inside one CTA's range is
+// written directly; a sequence cut by range boundaries leaves one partial
+// (max, sum, accumulator) per CTA, merged by the combine kernel.  Every CTA gets
+// the same number of tiles to within one, whatever the length mix.
+//
+// Roles (192 threads, one CTA per SM): warp 0 issues TMA, warp 1 issues MMA,
+// warps 2-5 run the softmax and the epilogue.  All waits are bounded.
+#include <math_constants.h>
+
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+#include "pa_sm100.cuh"
+
+namespace pa {
+namespace {
+
+using namespace sm100;
+
+constexpr int kD = 128;
+constexpr int kRows = 128;                   // rows per tile (M of the S MMA)
+constexpr int kSlab = kRows * 128;           // 128 rows x 128 B
+constexpr int kStage = 2 * kSlab;            // one K or V tile
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+constexpr int kMaxStages = 6;
+constexpr int kSmemBudget = 232448 - 1024;   // per-block limit minus alignment slack
+constexpr int kTailReserve = 6 * 1024;
+
+template <int H, int G>
+struct Geo {
+  static constexpr int Hq = H * G;
+  static constexpr int N = (Hq + 15) / 16 * 16;
+  static constexpr int TT = kRows / H;                   // tokens per tile
+  static constexpr int kQBytes = N * 256;
+  static constexpr int kQBufs = N >= 64 ? 1 : 2;         // one buffer leaves room for a 4th stage
+  static constexpr int kPHalf = N * 256;
+  static constexpr int kPBytes = 2 * kPHalf;
+  // as many 32 KB ring stages as the shared memory left over allows
+  static constexpr int kFree = kSmemBudget - kTailReserve - kQBufs * kQBytes - 2 * kPBytes;
+  static constexpr int kStages = kFree / kStage > kMaxStages ? kMaxStages : kFree / kStage;
+  static constexpr uint32_t kTmemCols = 4 * N < 64 ? 64 : 4 * N;
+  static constexpr int kRingOff = 0;
+  static constexpr int kQOff = kStages * kStage;
+  static constexpr int kPOff = kQOff + kQBufs * kQBytes;
+  static constexpr int kTailOff = kPOff + 2 * kPBytes;
+};
+
+struct SegInfo {
+  int b, L, j0, j1;       // sequence, its length, tile range [j0, j1) within it
+  int direct, slot;       // direct output, or partial slot 0/1 of this CTA
+  int valid, pad;
+};
+
+template <int N>
+struct Tail {
+  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t seg_full[2], seg_empty[2];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full[2], p_empty[2];
+  uint64_t o_full[2], o_empty[2];
+  uint64_t red[2], lsum, drain;
+  SegInfo seg[2];
+  float red_buf[2][4][N];
+  float alpha[2][N];
+  float lred[4][N];
+  float m_fin[N];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int DT, int H, int G>
+constexpr int smem_bytes() {
+  return Geo<H, G>::kTailOff + (int)sizeof(Tail<Geo<H, G>::N>) + 1024;
+}
+
+struct SkParams {
+  DecodeParams p;
+  const int* tile_prefix;   // [B + 1] tiles before sequence b
+  const int* first_seq;     // [grid] sequence holding each CTA's first tile
+  const int* total_tiles;   // [1]
+  float* part_m;            // [grid * 2 * Hq]
+  float* part_l;
+  float* part_acc;          // [grid * 2 * Hq * D]
+};
+
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
+  const int L = p.seq_lens[b];
+  return L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+}
+
+__device__ __forceinline__ int range_start(int c, int T, int grid) {
+  return (int)((long long)c * T / grid);
+}
+
+template <int DT, int H, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const SkParams sp) {
+  using Gm = Geo<H, G>;
+  constexpr int N = Gm::N, TT = Gm::TT, S = Gm::kStages;
+  static_assert(S >= 3, "ring too shallow");
+  static_assert(Gm::kTailOff + (int)sizeof(Tail<N>) <= kSmemBudget, "shared memory layout");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  Tail<N>* tl = reinterpret_cast<Tail<N>*>(smem + Gm::kTailOff);
+  volatile int* abort_flag = &tl->abort_flag;
+  const DecodeParams& p = sp.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = *sp.total_tiles;
+  const int c = blockIdx.x, grid = gridDim.x;
+  const int t_begin = range_start(c, T, grid), t_end = range_start(c + 1, T, grid);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&tl->full[s], 1);
+      mbar_init(&tl->empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tl->seg_full[i], 1);
+      mbar_init(&tl->seg_empty[i], 5);
+      mbar_init(&tl->q_full[i], 1);
+      mbar_init(&tl->q_empty[i], 1);
+      mbar_init(&tl->s_full[i], 1);
+      mbar_init(&tl->s_empty[i], 4);
+      mbar_init(&tl->p_full[i], 4);
+      mbar_init(&tl->p_empty[i], 1);
+      mbar_init(&tl->o_full[i], 1);
+      mbar_init(&tl->o_empty[i], 4);
+      mbar_init(&tl->red[i], 4);
+    }
+    mbar_init(&tl->lsum, 4);
+    mbar_init(&tl->drain, 1);
+    tl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tl->tmem_base, Gm::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp >= 2) {
+    // P' is block diagonal: entries outside a row's query group stay zero forever
+    uint4* pz = reinterpret_cast<uint4*>(smem + Gm::kPOff);
+    for (int i = threadIdx.x - 64; i < 2 * Gm::kPBytes / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tl->tmem_base;
+  const uint32_t ring_addr = smem_addr(smem + Gm::kRingOff);
+  const uint32_t q_addr = smem_addr(smem + Gm::kQOff);
+  const uint32_t p_addr = smem_addr(smem + Gm::kPOff);
+
+  auto set_abort = [&]() {
+    tl->abort_flag = 1;
+    report(p.status_dev, PA_ERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- producer --
+    const uint64_t policy = policy_evict_first();
+    int stage = 0, sphase = 0;
+    int issued[kMaxStages] = {-1, -1, -1, -1, -1, -1};
+    int q_issued[2] = {-1, -1};
+    int seg_idx = 0;
+    bool ok = true;
+    int tile = t_begin;
+    int b = t_begin < t_end ? sp.first_seq[c] : 0;
+    while (ok) {
+      SegInfo sg;
+      sg.valid = 0;
+      int tpb = 0;
+      if (tile < t_end) {
+        int tpb1;
+        for (;;) {                       // skip sequences without tiles
+          tpb = sp.tile_prefix[b];
+          tpb1 = sp.tile_prefix[b + 1];
+          if (tpb1 > tile) break;
+          ++b;
+        }
+        sg.b = b;
+        sg.L = clamp_len(p, b);
+        sg.j0 = tile - tpb;
+        sg.j1 = min(t_end, tpb1) - tpb;
+        sg.direct = (sg.j0 == 0 && sg.j1 == tpb1 - tpb);
+        sg.slot = seg_idx == 0 ? 0 : 1;
+        sg.valid = 1;
+      }
+      const int islot = seg_idx & 1;
+      if (lane == 0) {
+        ok = mbar_wait(&tl->seg_empty[islot], ((seg_idx >> 1) & 1) ^ 1, abort_flag, kWaitNs);
+        if (ok) {
+          tl->seg[islot] = sg;
+          mbar_arrive(&tl->seg_full[islot]);
+        } else {
+          set_abort();
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
+      if (!ok || !sg.valid) break;
+      // all query heads of the sequence (N rows; rows past Hq are never used)
+      const int qb = seg_idx % Gm::kQBufs, qph = (seg_idx / Gm::kQBufs) & 1;
+      if (lane == 0) {
+        ok = mbar_wait(&tl->q_empty[qb], qph ^ 1, abort_flag, kWaitNs);
+        if (ok) {
+          mbar_arrive_expect_tx(&tl->q_full[qb], Gm::kQBytes);
+          tma_load_2d(smem + Gm::kQOff + qb * Gm::kQBytes, &tm_q, &tl->q_full[qb], 0, sg.b * p.Hq);
+          tma_load_2d(smem + Gm::kQOff + qb * Gm::kQBytes + N * 128, &tm_q, &tl->q_full[qb], 64,
+                      sg.b * p.Hq);
+          q_issued[qb] = qph;
+        } else {
+          set_abort();
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
+      if (!ok) break;
+      // block ids of this segment, 32 per chunk held one per lane, next chunk prefetched
+      const int32_t* table = p.block_tables + (int64_t)sg.b * p.max_blocks;
+      const int nblk_seq = (sg.L + p.bs - 1) / p.bs;
+      const int k_first = (sg.j0 * TT) / p.bs;
+      int kb = k_first;
+      auto load_chunk = [&](int base) -> int32_t {
+        const int k = base + lane;
+        int32_t id = 0;
+        if (k < nblk_seq) {
+          id = table[k];
+          if (p.status_dev && (id < 0 || id >= p.num_blocks)) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+        }
+        return id;
+      };
+      int32_t cur = load_chunk(kb), nxt = load_chunk(kb + 32);
+      for (int j = sg.j0; j < sg.j1 && ok; ++j) {
+        const int tok0 = j * TT;
+        int k0, nops, box_tokens, tok_off;
+        if (TT >= p.bs) {
+          k0 = tok0 / p.bs;
+          nops = min(TT / p.bs, nblk_seq - k0);
+          box_tokens = p.bs;
+          tok_off = 0;
+        } else {
+          k0 = tok0 / p.bs;
+          nops = 1;
+          box_tokens = TT;
+          tok_off = tok0 % p.bs;
+        }
+        while (k0 - kb >= 32) {          // advance the id window
+          kb += 32;
+          cur = nxt;
+          nxt = load_chunk(kb + 32);
+        }
+        const uint32_t bytes = (uint32_t)nops * box_tokens * H * 128u * 2u;
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          if (lane == 0) {
+            ok = mbar_wait(&tl->empty[stage], sphase ^ 1, abort_flag, kWaitNs);
+            if (ok) mbar_arrive_expect_tx(&tl->full[stage], bytes);
+            else set_abort();
+          }
+          ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
+          if (!ok) break;
+          const int src = k0 + (lane < nops ? lane : 0) - kb;
+          const int32_t a = __shfl_sync(0xFFFFFFFFu, cur, src & 31);
+          const int32_t bb = __shfl_sync(0xFFFFFFFFu, nxt, src & 31);
+          const int32_t blk = src < 32 ? a : bb;
+          if (lane < nops) {
+            const CUtensorMap* map = kv == 0 ? &tm_k : &tm_v;
+            uint8_t* dst = smem + Gm::kRingOff + stage * kStage + lane * box_tokens * H * 128;
+            const int row = blk * p.bs + tok_off;
+            tma_load_3d_hint(dst, map, &tl->full[stage], 0, 0, row, policy);
+            tma_load_3d_hint(dst + kSlab, map, &tl->full[stage], 64, 0, row, policy);
+          }
+          issued[stage] = sphase;
+          if (++stage == S) {
+            stage = 0;
+            sphase ^= 1;
+          }
+        }
+      }
+      if (!ok) break;
+      tile = tpb + sg.j1;
+      ++b;
+      ++seg_idx;
+      __syncwarp();
+    }
+    if (*abort_flag && lane == 0) {
+      for (int s = 0; s < S; ++s)
+        if (issued[s] >= 0) mbar_wait_drain(&tl->full[s], issued[s], kWaitNs);
+      for (int i = 0; i < 2; ++i)
+        if (q_issued[i] >= 0) mbar_wait_drain(&tl->q_full[i], q_issued[i], kWaitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue --
+    constexpr uint32_t ab = DT == PA_BFLOAT16 ? 1u : 0u;
+    constexpr uint32_t idesc_s = idesc_f16(ab, 0, 0, kRows, N);
+    constexpr uint32_t idesc_o = idesc_f16(ab, 1, 0, kD, N);
+    int stage = 0, sphase = 0, tile_g = 0, seg_idx = 0;
+    bool ok = true, committed = false;
+    auto issue_pv = [&](int t, int vs, int vph) -> bool {
+      const int slot = t & 1, ph = (t >> 1) & 1;
+      if (!mbar_wait(&tl->full[vs], vph, abort_flag, kWaitNs)) return false;
+      if (!mbar_wait(&tl->p_full[slot], ph, abort_flag, kWaitNs)) return false;
+      if (!mbar_wait(&tl->o_empty[slot], ph ^ 1, abort_flag, kWaitNs)) return false;
+      tc_fence_after();
+      const uint32_t vaddr = ring_addr + vs * kStage;
+      const uint32_t paddr = p_addr + slot * Gm::kPBytes;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(vaddr + kk * 16 * 128, kSlab, 1024);
+          const uint64_t bd = smem_desc_sw128(
+              paddr + half * Gm::kPHalf + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
+          mma_f16(tmem + 2 * N + slot * N, a, bd, idesc_o, (half | kk) != 0);
+        }
+      }
+      mma_commit(&tl->empty[vs]);
+      mma_commit(&tl->o_full[slot]);
+      mma_commit(&tl->p_empty[slot]);
+      return true;
+    };
+    for (;;) {
+      const int islot = seg_idx & 1;
+      int valid = 0, ntiles = 0;
+      if (lane == 0) {
+        ok = mbar_wait(&tl->seg_full[islot], (seg_idx >> 1) & 1, abort_flag, kWaitNs);
+        if (ok) {
+          valid = tl->seg[islot].valid;
+          ntiles = tl->seg[islot].j1 - tl->seg[islot].j0;
+          mbar_arrive(&tl->seg_empty[islot]);
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
+      valid = __shfl_sync(0xFFFFFFFFu, valid, 0);
+      ntiles = __shfl_sync(0xFFFFFFFFu, ntiles, 0);
+      if (!ok) {
+        if (lane == 0) set_abort();
+        break;
+      }
+      if (!valid) break;
+      const int qb = seg_idx % Gm::kQBufs;
+      if (lane == 0) {
+        ok = mbar_wait(&tl->q_full[qb], (seg_idx / Gm::kQBufs) & 1, abort_flag, kWaitNs);
+        int pvs = 0, pvph = 0;
+        for (int j = 0; j < ntiles && ok; ++j) {
+          const int t = tile_g + j;
+          const int slot = t & 1, ph = (t >> 1) & 1;
+          const int ks = stage, kph = sphase;
+          if (++stage == S) { stage = 0; sphase ^= 1; }
+          const int vs = stage, vph = sphase;
+          if (++stage == S) { stage = 0; sphase ^= 1; }
+          ok = mbar_wait(&tl->full[ks], kph, abort_flag, kWaitNs) &&
+               mbar_wait(&tl->s_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kaddr = ring_addr + ks * kStage;
+          const uint32_t qaddr = q_addr + qb * Gm::kQBytes;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * (N * 128) + (kk & 3) * 32;
+            mma_f16(tmem + slot * N, smem_desc_sw128(kaddr + off, 16, 1024),
+                    smem_desc_sw128(qaddr + qoff, 16, 1024), idesc_s, kk > 0);
+          }
+          mma_commit(&tl->empty[ks]);
+          mma_commit(&tl->s_full[slot]);
+          if (j == ntiles - 1) mma_commit(&tl->q_empty[qb]);
+          committed = true;
+          if (j > 0) ok = issue_pv(t - 1, pvs, pvph);
+          pvs = vs;
+          pvph = vph;
+        }
+        if (ok) ok = issue_pv(tile_g + ntiles - 1, pvs, pvph);
+        if (!ok) set_abort();
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
+      if (!ok) break;
+      tile_g += ntiles;
+      ++seg_idx;
+    }
+    if (*abort_flag && lane == 0 && committed) {
+      mma_commit(&tl->drain);
+      mbar_wait_drain(&tl->drain, 0, kWaitNs);
+    }
+  } else {
+    // ------------------------------------------------- softmax / epilogue --
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;            // tile row (token r / H, head r % H); O row d
+    const int tt = r / H, h = lane % H;      // H divides 32
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    int tile_g = 0, seg_idx = 0, round = 0, lround = 0;
+    bool ok = true;
+    auto wait_all = [&](uint64_t* bar, int parity) -> bool {
+      const bool w = mbar_wait(bar, parity, abort_flag, kWaitNs);
+      return __all_sync(0xFFFFFFFFu, w);
+    };
+    for (;;) {
+      const int islot = seg_idx & 1;
+      if (!wait_all(&tl->seg_full[islot], (seg_idx >> 1) & 1)) { ok = false; break; }
+      const SegInfo sg = tl->seg[islot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tl->seg_empty[islot]);
+      if (!sg.valid) break;
+      const int ntiles = sg.j1 - sg.j0;
+      float m_run[G], l_t[G], acc[N];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        m_run[g] = -CUDART_INF_F;
+        l_t[g] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < N; ++q) acc[q] = 0.f;
+      // acc <- acc * alpha(t) + O_t, alpha(t) from round `rnd` (all query heads)
+      auto accumulate = [&](int t, int rnd) -> bool {
+        const int slot = t & 1, ph = (t >> 1) & 1;
+        if (!wait_all(&tl->o_full[slot], ph)) return false;
+        tc_fence_after();
+        const float* al = tl->alpha[rnd & 1];
+#pragma unroll
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float o[16];
+          tmem_ld16(tmem + lane_base + 2 * N + slot * N + c0, o);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(acc[c0 + i], al[c0 + i], o[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->o_empty[slot]);
+        return true;
+      };
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int t = tile_g + j;
+        const int slot = t & 1, ph = (t >> 1) & 1;
+        if (!wait_all(&tl->s_full[slot], ph)) { ok = false; break; }
+        tc_fence_after();
+        float x[G];
+        {
+          float s[N];
+#pragma unroll
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + slot * N + c0, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s[c0 + i] = v[i];
+          }
+#pragma unroll
+          for (int hh = 0; hh < H; ++hh)
+            if (h == hh) {
+#pragma unroll
+              for (int g = 0; g < G; ++g) x[g] = s[hh * G + g];
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->s_empty[slot]);
+        const bool valid = (sg.j0 + j) * TT + tt < sg.L;
+        float wm[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          x[g] = valid ? x[g] * p.scale_log2 : -CUDART_INF_F;
+          wm[g] = x[g];
+        }
+        // rows of the same KV head in this warp: lanes h, h+H, ... (xor H .. 16)
+#pragma unroll
+        for (int off = H; off < 32; off <<= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) wm[g] = fmaxf(wm[g], __shfl_xor_sync(0xFFFFFFFFu, wm[g], off));
+        const int rb = round & 1;
+        if (lane < H)
+#pragma unroll
+          for (int g = 0; g < G; ++g) tl->red_buf[rb][wq][h * G + g] = wm[g];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->red[rb]);
+        if (!wait_all(&tl->red[rb], (round >> 1) & 1)) { ok = false; break; }
+        float alpha[G], pr[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int q = h * G + g;
+          const float tm = fmaxf(fmaxf(tl->red_buf[rb][0][q], tl->red_buf[rb][1][q]),
+                                 fmaxf(tl->red_buf[rb][2][q], tl->red_buf[rb][3][q]));
+          const float m_new = fmaxf(m_run[g], tm);
+          alpha[g] = exp2f(m_run[g] - m_new);
+          pr[g] = valid ? exp2f(x[g] - m_new) : 0.f;
+          l_t[g] = fmaf(l_t[g], alpha[g], pr[g]);
+          m_run[g] = m_new;
+        }
+        if (wq == 0 && lane < H) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) tl->alpha[rb][h * G + g] = alpha[g];
+        }
+        // P' entries of this row: (head h*G+g, column r)
+        if (!wait_all(&tl->p_empty[slot], ph ^ 1)) { ok = false; break; }
+        uint8_t* pbuf = smem + Gm::kPOff + slot * Gm::kPBytes + (r >> 6) * (N * 128);
+        const int chunk = (r & 63) >> 3;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int q = h * G + g;
+          const uint16_t hi = narrow<DT>(pr[g]);
+          const uint16_t lo = narrow<DT>(pr[g] - widen2<DT>(hi).x);
+          const int off = q * 128 + ((chunk ^ (q & 7)) << 4) + (r & 7) * 2;
+          *reinterpret_cast<uint16_t*>(pbuf + off) = hi;
+          *reinterpret_cast<uint16_t*>(pbuf + Gm::kPHalf + off) = lo;
+        }
+        // rows of tokens past the end: zero their V row (0 * garbage must not reach O)
+        if ((sg.j0 + j + 1) * TT > sg.L) {
+          const int u = 2 * t + 1;
+          const int vs = u % S, vph = (u / S) & 1;
+          if (!wait_all(&tl->full[vs], vph)) { ok = false; break; }
+          if (!valid) {
+            uint4* r0 = reinterpret_cast<uint4*>(smem + Gm::kRingOff + vs * kStage + r * 128);
+            uint4* r1 = reinterpret_cast<uint4*>(smem + Gm::kRingOff + vs * kStage + kSlab + r * 128);
+            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              r0[i] = z;
+              r1[i] = z;
+            }
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->p_full[slot]);
+        if (j > 0 && !accumulate(t - 1, round - 1)) { ok = false; break; }
+        ++round;
+      }
+      if (!ok) break;
+      // denominators (and final maxima) of the segment, per query head
+      {
+        float ls[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) ls[g] = l_t[g];
+#pragma unroll
+        for (int off = H; off < 32; off <<= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) ls[g] += __shfl_xor_sync(0xFFFFFFFFu, ls[g], off);
+        if (lane < H)
+#pragma unroll
+          for (int g = 0; g < G; ++g) tl->lred[wq][h * G + g] = ls[g];
+        if (wq == 0 && lane < H)
+#pragma unroll
+          for (int g = 0; g < G; ++g) tl->m_fin[h * G + g] = m_run[g];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->lsum);
+        if (!wait_all(&tl->lsum, lround & 1)) { ok = false; break; }
+        ++lround;
+      }
+      if (!accumulate(tile_g + ntiles - 1, round - 1)) { ok = false; break; }
+      const int Hq = p.Hq;
+#pragma unroll
+      for (int q = 0; q < N; ++q) {
+        if (q < Hq) {
+          const float l = tl->lred[0][q] + tl->lred[1][q] + tl->lred[2][q] + tl->lred[3][q];
+          if (sg.direct) {
+            static_cast<uint16_t*>(p.out)[((int64_t)sg.b * Hq + q) * kD + r] = narrow<DT>(acc[q] / l);
+          } else {
+            const int64_t idx = ((int64_t)c * 2 + sg.slot) * Hq + q;
+            sp.part_acc[idx * kD + r] = acc[q];
+            if (r == 0) {
+              sp.part_m[idx] = tl->m_fin[q];
+              sp.part_l[idx] = l;
+            }
+          }
+        }
+      }
+      tile_g += ntiles;
+      ++seg_idx;
+    }
+    if (!ok) set_abort();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Gm::kTmemCols);
+  }
+}
+
+// Tile prefix over the sequences, the first sequence of every CTA's range,
+// zero rows for empty sequences.  One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024)
+plan_sk_kernel(const DecodeParams p, int TT, int grid, int* tile_prefix, int* first_seq,
+               int* total_tiles) {
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (p.B + 1023) / 1024;
+  const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
+  int mine = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int raw = p.seq_lens[b];
+    if (raw < 0 || raw > p.max_seq_len) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+    mine += (clamp_len(p, b) + TT - 1) / TT;
+  }
+  int inc = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int v = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, v, o);
+      if (lane >= o) v += u;
+    }
+    warp_tot[lane] = v;
+  }
+  __syncthreads();
+  int run = inc - mine + (warp ? warp_tot[warp - 1] : 0);
+  for (int b = b0; b < b1; ++b) {
+    tile_prefix[b] = run;
+    const int L = clamp_len(p, b);
+    run += (L + TT - 1) / TT;
+    if (L == 0) {
+      uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)b * p.Hq * p.D;
+      for (int e = 0; e < p.Hq * p.D; ++e) o[e] = 0;
+    }
+  }
+  const int T = warp_tot[31];
+  if (tid == 0) {
+    tile_prefix[p.B] = T;
+    *total_tiles = T;
+  }
+  __syncthreads();
+  __threadfence_block();
+  // first sequence of each CTA: the b with prefix[b] <= start < prefix[b+1]
+  for (int cc = tid; cc < grid; cc += 1024) {
+    const int start = range_start(cc, T, grid);
+    int lo = 0, hi = p.B - 1;
+    if (T == 0) {
+      first_seq[cc] = 0;
+      continue;
+    }
+    while (lo < hi) {        // last b with tile_prefix[b] <= start
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_prefix[mid] <= start) lo = mid;
+      else hi = mid - 1;
+    }
+    first_seq[cc] = lo;
+  }
+}
+
+// Merge the partials of sequences cut by CTA range boundaries.  One warp per
+// (sequence, query head).
+template <int DT>
+__global__ void __launch_bounds__(128)
+combine_sk_kernel(const SkParams sp, int grid) {
+  const DecodeParams& p = sp.p;
+  constexpr int PER = kD / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 4 + warp;
+  if (row >= (int64_t)p.B * p.Hq) return;
+  const int b = (int)(row / p.Hq), q = (int)(row - (int64_t)b * p.Hq);
+  const int T = *sp.total_tiles;
+  const int tpb = sp.tile_prefix[b], tpb1 = sp.tile_prefix[b + 1];
+  if (tpb1 <= tpb) return;                                  // empty: zeroed by the plan
+  auto owner = [&](int x) { return (int)(((long long)(x + 1) * grid - 1) / T); };
+  const int cf = owner(tpb), cl = owner(tpb1 - 1);
+  if (cf == cl) return;                                     // written directly
+  // CTAs whose range is empty (fewer tiles than CTAs) wrote no partial
+  float M = -CUDART_INF_F;
+  for (int cc = cf + lane; cc <= cl; cc += 32) {
+    const int st = range_start(cc, T, grid);
+    if (st == range_start(cc + 1, T, grid)) continue;
+    const int slot = st >= tpb ? 0 : 1;
+    M = fmaxf(M, sp.part_m[((int64_t)cc * 2 + slot) * p.Hq + q]);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+  float den = 0.f, o_acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) o_acc[i] = 0.f;
+  for (int cc = cf; cc <= cl; ++cc) {
+    const int st = range_start(cc, T, grid);
+    if (st == range_start(cc + 1, T, grid)) continue;
+    const int slot = st >= tpb ? 0 : 1;
+    const int64_t idx = ((int64_t)cc * 2 + slot) * p.Hq + q;
+    const float w = exp2f(sp.part_m[idx] - M);
+    den = fmaf(w, sp.part_l[idx], den);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o_acc[i] = fmaf(w, sp.part_acc[idx * kD + lane * PER + i], o_acc[i]);
+  }
+  const float inv = 1.f / den;
+  uint16_t* out = static_cast<uint16_t*>(p.out) + row * kD + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) out[i] = narrow<DT>(o_acc[i] * inv);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int DT, int H, int G>
+pa_status launch_t(const SkParams& sp, const CUtensorMap& k, const CUtensorMap& v,
+                   const CUtensorMap& q, int grid, cudaStream_t stream) {
+  constexpr int bytes = smem_bytes<DT, H, G>();
+  static_assert(bytes <= 232448, "shared memory over the per-block limit");
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(decode_tcg_kernel<DT, H, G>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
+  if (attr != cudaSuccess) return PA_ERR_CUDA;
+  decode_tcg_kernel<DT, H, G><<<grid, kThreads, bytes, stream>>>(k, v, q, sp);
+  PA_CHECK_LAUNCH();
+  return PA_OK;
+}
+
+template <int DT, int H>
+pa_status launch_h(int G, const SkParams& sp, const CUtensorMap& k, const CUtensorMap& v,
+                   const CUtensorMap& q, int grid, cudaStream_t stream) {
+  switch (G) {
+    case 1: return launch_t<DT, H, 1>(sp, k, v, q, grid, stream);
+    case 2: return launch_t<DT, H, 2>(sp, k, v, q, grid, stream);
+    case 4: return launch_t<DT, H, 4>(sp, k, v, q, grid, stream);
+    case 8: return launch_t<DT, H, 8>(sp, k, v, q, grid, stream);
+    default: return PA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+bool tcg_supported(const DecodeParams& p) {
+  const int G = p.Hq / p.Hkv;
+  if (p.D != kD) return false;
+  if (p.Hkv != 4 && p.Hkv != 8) return false;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+  if ((long long)p.num_blocks * p.bs >= (1ll << 31)) return false;
+  if ((long long)p.B * p.Hq >= (1ll << 31)) return false;
+  return encode_fn() != nullptr;
+}
+
+SkLayout sk_layout(int B, int Hq) {
+  auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  SkLayout l;
+  l.prefix_off = 0;
+  l.first_off = l.prefix_off + a((size_t)(B + 1) * sizeof(int));
+  l.total_off = l.first_off + a((size_t)kSkMaxGrid * sizeof(int));
+  l.m_off = l.total_off + 256;
+  const size_t parts = (size_t)kSkMaxGrid * 2 * Hq;
+  l.l_off = l.m_off + a(parts * sizeof(float));
+  l.acc_off = l.l_off + a(parts * sizeof(float));
+  l.total = l.acc_off + a(parts * kD * sizeof(float));
+  return l;
+}
+
+pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t stream) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PA_ERR_UNSUPPORTED;
+  const int H = p.Hkv, G = p.Hq / p.Hkv;
+  const int TT = kRows / H;
+  const int N = (p.Hq + 15) / 16 * 16;
+  const CUtensorMapDataType dt =
+      p.dtype == PA_BFLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int box_tokens = p.bs < TT ? p.bs : TT;
+  CUtensorMap tk, tv, tq;
+  const cuuint64_t kv_dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)p.num_blocks * p.bs};
+  const cuuint64_t kv_strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+  const cuuint32_t kv_box[3] = {64, (cuuint32_t)H, (cuuint32_t)box_tokens};
+  const cuuint32_t ones[3] = {1, 1, 1};
+  if (enc(&tk, dt, 3, const_cast<void*>(p.k_pool), kv_dims, kv_strides, kv_box, ones,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PA_ERR_INVALID_ARG;
+  if (enc(&tv, dt, 3, const_cast<void*>(p.v_pool), kv_dims, kv_strides, kv_box, ones,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PA_ERR_INVALID_ARG;
+  const cuuint64_t q_dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.B * p.Hq};
+  const cuuint64_t q_strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t q_box[2] = {64, (cuuint32_t)N};
+  if (enc(&tq, dt, 2, const_cast<void*>(p.q), q_dims, q_strides, q_box, ones,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PA_ERR_INVALID_ARG;
+
+  int grid = device_sms();
+  if (grid <= 0) return PA_ERR_CUDA;
+  if (grid > kSkMaxGrid) grid = kSkMaxGrid;
+  const SkLayout l = sk_layout(p.B, p.Hq);
+  char* ws = static_cast<char*>(sk_ws);
+  SkParams sp;
+  sp.p = p;
+  sp.tile_prefix = reinterpret_cast<int*>(ws + l.prefix_off);
+  sp.first_seq = reinterpret_cast<int*>(ws + l.first_off);
+  sp.total_tiles = reinterpret_cast<int*>(ws + l.total_off);
+  sp.part_m = reinterpret_cast<float*>(ws + l.m_off);
+  sp.part_l = reinterpret_cast<float*>(ws + l.l_off);
+  sp.part_acc = reinterpret_cast<float*>(ws + l.acc_off);
+
+  plan_sk_kernel<<<1, 1024, 0, stream>>>(p, TT, grid, const_cast<int*>(sp.tile_prefix),
+                                         const_cast<int*>(sp.first_seq),
+                                         const_cast<int*>(sp.total_tiles));
+  PA_CHECK_LAUNCH();
+  pa_status st;
+  if (p.dtype == PA_BFLOAT16)
+    st = H == 4 ? launch_h<PA_BFLOAT16, 4>(G, sp, tk, tv, tq, grid, stream)
+                : launch_h<PA_BFLOAT16, 8>(G, sp, tk, tv, tq, grid, stream);
+  else
+    st = H == 4 ? launch_h<PA_FLOAT16, 4>(G, sp, tk, tv, tq, grid, stream)
+                : launch_h<PA_FLOAT16, 8>(G, sp, tk, tv, tq, grid, stream);
+  if (st != PA_OK) return st;
+  const long long rows = (long long)p.B * p.Hq;
+  if (rows == 0) return PA_OK;
+  const unsigned cgrid = (unsigned)((rows + 3) / 4);
+  if (p.dtype == PA_BFLOAT16) combine_sk_kernel<PA_BFLOAT16><<<cgrid, 128, 0, stream>>>(sp, grid);
+  else combine_sk_kernel<PA_FLOAT16><<<cgrid, 128, 0, stream>>>(sp, grid);
+  PA_CHECK_LAUNCH();
+  return PA_OK;
+}
+
+}  // namespace pa

@@ -29,15 +29,26 @@ struct DecodeParams {
 
 // Workspace carve-up; identical for every decode kernel.
 struct WorkspaceLayout {
-  size_t queue_off, items_off, m_off, l_off, acc_off, total;
+  size_t queue_off, items_off, m_off, l_off, acc_off, sk_off, total;
 };
 WorkspaceLayout workspace_layout(int B, int Hq, int D, int P);
 
 pa_status launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 pa_status launch_combine(const DecodeParams& p, cudaStream_t stream);
 
-// Tensor-core path (head_dim 128): plan kernel + persistent tcgen05 kernel.
+// Tensor-core path, one KV head per work item (head_dim 128): plan kernel +
+// persistent tcgen05 kernel; partials go to the [B, Hq, P] workspace arrays.
 bool tc_supported(const DecodeParams& p);
 pa_status launch_decode_tc(const DecodeParams& p, int2* items, int* queue, cudaStream_t stream);
+
+// Tensor-core path, all KV heads of a block per CTA with a stream-K split
+// (head_dim 128, Hkv 4 or 8, G in {1,2,4,8}): plan + main + combine kernels.
+constexpr int kSkMaxGrid = 160;          // persistent CTAs at most (GB300: 152 SMs)
+struct SkLayout {
+  size_t prefix_off, first_off, total_off, m_off, l_off, acc_off, total;
+};
+SkLayout sk_layout(int B, int Hq);
+bool tcg_supported(const DecodeParams& p);
+pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t stream);
 
 }  // namespace pa

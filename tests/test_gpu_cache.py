@@ -13,9 +13,11 @@ from tests.gpu_helpers import DeviceBatch, assert_close, i32, lib, to_dev, to_ho
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=["simt", "tc"])
+@pytest.fixture(scope="module", params=["simt", "tc_head", "tc"])
 def pa(request):
-    """Every test runs on the CUDA-core and on the tensor-core decode kernel."""
+    """Every test runs on each decode kernel: CUDA cores, the per-head
+    tensor-core kernel and the grouped tensor-core kernel (for shapes it does
+    not serve, "tc" runs the per-head one)."""
     m = lib()
     m.set_decode_path(request.param)
     m.decode_path = request.param
@@ -24,7 +26,7 @@ def pa(request):
 
 
 def needs(pa, head_dim):
-    if pa.decode_path == "tc" and head_dim != 128:
+    if pa.decode_path != "simt" and head_dim != 128:
         pytest.skip("the tensor-core kernel serves head_dim 128")
 
 

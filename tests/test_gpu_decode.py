@@ -19,9 +19,11 @@ from tests.gpu_helpers import DeviceBatch, assert_close, i32, lib, to_dev, to_ho
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=["simt", "tc"])
+@pytest.fixture(scope="module", params=["simt", "tc_head", "tc"])
 def pa(request):
-    """Every test runs on the CUDA-core and on the tensor-core decode kernel."""
+    """Every test runs on each decode kernel: CUDA cores, the per-head
+    tensor-core kernel and the grouped tensor-core kernel (for shapes it does
+    not serve, "tc" runs the per-head one)."""
     m = lib()
     m.set_decode_path(request.param)
     m.decode_path = request.param
@@ -30,7 +32,7 @@ def pa(request):
 
 
 def needs(pa, head_dim):
-    if pa.decode_path == "tc" and head_dim != 128:
+    if pa.decode_path != "simt" and head_dim != 128:
         pytest.skip("the tensor-core kernel serves head_dim 128")
 
 
@@ -105,6 +107,23 @@ def test_query_groupings(pa, hq, hkv):
     batch = scenarios.fixed_batch(w)
     got = widen(DeviceBatch(batch).decode(pa))
     assert_close(got, scenarios.decode_f64(batch), f"Hq={hq} Hkv={hkv}")
+
+
+@pytest.mark.parametrize("hkv,hq,bs,lens", [
+    (8, 32, 16, (100,)),                 # fewer tiles than SMs: most CTAs idle
+    (4, 16, 32, (128, 300)),
+    (4, 4, 64, (513, 77)),
+    (8, 64, 8, (1, 2, 3)),
+    (8, 32, 16, tuple(range(1, 400, 7))),  # many short sequences per CTA
+])
+def test_small_and_many_short_batches(pa, hkv, hq, bs, lens):
+    """Batches with fewer token tiles than SMs, and CTAs spanning many short
+    sequences: the work split must still cover every token exactly once."""
+    w = _small("llama3_8b", num_seqs=len(lens), num_q_heads=hq, num_kv_heads=hkv, block_size=bs,
+               length_kind="fixed", lens=tuple(lens), seed=31 + hq + bs)
+    batch = scenarios.fixed_batch(w)
+    got = widen(DeviceBatch(batch).decode(pa))
+    assert_close(got, scenarios.decode_f64(batch), f"Hkv={hkv} Hq={hq} bs={bs} B={len(lens)}")
 
 
 @pytest.mark.parametrize("pt", [128, 256, 512, 1024])
