@@ -172,9 +172,13 @@ def recorded_traffic(workload_name: str):
 
 
 def decode_kernel_for(w, kernel: str) -> str:
-    """Which decode kernel runs: the tensor-core kernel serves head_dim 128."""
-    if kernel == "auto":
-        return "tc" if w.head_dim == 128 else "simt"
+    """Which decode kernel runs (mirrors the library's selection)."""
+    grouped = (w.head_dim == 128 and w.num_kv_heads in (4, 8) and w.group in (1, 2, 4, 8)
+               and w.num_seqs <= 1023)
+    if kernel in ("auto", "tc"):
+        if grouped:
+            return "tcg"
+        return "tc_head" if w.head_dim == 128 else "simt"
     return kernel
 
 
@@ -221,7 +225,12 @@ class NativeStep:
         # decode_slots + reshape_and_cache + decode (+ plan on the tensor-core
         # path) + combine when a sequence spans several partitions
         self.kernel = decode_kernel_for(w, kernel)
-        self.launches_per_step = 3 + (1 if self.kernel == "tc" else 0) + (1 if P > 1 else 0)
+        if self.kernel == "tcg":      # main + combine
+            self.launches_per_step = 2 + 2
+        elif self.kernel == "tc_head":  # plan + main (+ combine)
+            self.launches_per_step = 2 + 2 + (1 if P > 1 else 0)
+        else:                           # main (+ combine)
+            self.launches_per_step = 2 + 1 + (1 if P > 1 else 0)
         # pinned host copies for the end-to-end measurement
         self.h_q = self.q.cpu().pin_memory()
         self.h_key = self.key.cpu().pin_memory()
@@ -361,7 +370,8 @@ def run_native(args, dist_info):
             "l2": f"inputs larger than L2: {kvb / 2**20:.0f} MiB of K/V read per step vs "
                   f"{L2_BYTES / 2**20:.0f} MiB L2; no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-            "decode_kernel": {"tc": "tcgen05 + TMA (decode_tc_kernel)",
+            "decode_kernel": {"tcg": "tcgen05 + TMA, whole-block (decode_tcg_kernel)",
+                              "tc_head": "tcgen05 + TMA, per KV head (decode_tc_kernel)",
                               "simt": "CUDA cores (decode_simt_kernel)"}[step.kernel],
         },
         "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
@@ -376,8 +386,9 @@ def run_native(args, dist_info):
         },
         "gpu_launches": step.launches_per_step * args.steps,
         "roofline": {
-            "kernel": "pa_decode (plan + split-K main + combine)" if step.kernel == "tc"
-                      else "pa_decode (split-K main + combine)",
+            "kernel": {"tcg": "pa_decode (stream-K main + combine)",
+                       "tc_head": "pa_decode (plan + split-K main + combine)",
+                       "simt": "pa_decode (split-K main + combine)"}[step.kernel],
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -563,7 +574,7 @@ def main():
                     choices=["llama3_8b", "long_context", "ragged", "tiny"])
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--partition-tokens", type=int, default=0)
-    ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_head"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()

@@ -29,6 +29,7 @@
 #include <math_constants.h>
 
 #include <mutex>
+#include <utility>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -48,7 +49,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 232448 - 1024;   // per-block limit minus alignment slack
-constexpr int kTailReserve = 6 * 1024;
+constexpr int kMaxSeqs = 1023;                 // batch size served (tile prefix in smem)
+constexpr int kTailReserve = 10 * 1024;
 
 template <int H, int G>
 struct Geo {
@@ -89,6 +91,8 @@ struct Tail {
   float alpha[2][N];
   float lred[4][N];
   float m_fin[N];
+  int prefix[kMaxSeqs + 1];   // tiles before sequence b; prefix[B] = all tiles
+  int scan[4];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -100,9 +104,7 @@ constexpr int smem_bytes() {
 
 struct SkParams {
   DecodeParams p;
-  const int* tile_prefix;   // [B + 1] tiles before sequence b
-  const int* first_seq;     // [grid] sequence holding each CTA's first tile
-  const int* total_tiles;   // [1]
+  int* tile_prefix;         // [B + 1] tiles before sequence b (written by CTA 0 for the combine)
   float* part_m;            // [grid * 2 * Hq]
   float* part_l;
   float* part_acc;          // [grid * 2 * Hq * D]
@@ -113,8 +115,21 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
   return L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
 }
 
+// First tile of CTA c's range (T tiles over `grid` CTAs; c * T < 2^31 here).
 __device__ __forceinline__ int range_start(int c, int T, int grid) {
-  return (int)((long long)c * T / grid);
+  return (int)((unsigned)c * (unsigned)T / (unsigned)grid);
+}
+
+// Wait until the kernel this launch depends on (previous in the stream) has
+// completed and its writes are visible; returns at once without such a launch.
+__device__ __forceinline__ void wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream (launched with programmatic serialization)
+// to be scheduled; it still waits for this grid to finish before reading.
+__device__ __forceinline__ void allow_next_grid() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <int DT, int H, int G>
@@ -133,9 +148,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
   volatile int* abort_flag = &tl->abort_flag;
   const DecodeParams& p = sp.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = *sp.total_tiles;
   const int c = blockIdx.x, grid = gridDim.x;
-  const int t_begin = range_start(c, T, grid), t_end = range_start(c + 1, T, grid);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -175,9 +188,49 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int i = threadIdx.x - 64; i < 2 * Gm::kPBytes / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
     fence_async_smem();
   }
+  allow_next_grid();
+  wait_prior_grid();           // inputs may come from the previous kernel in the stream
+  if (warp >= 2) {
+    // tile prefix over the batch (every CTA computes it; CTA 0 also stores it for
+    // the combine pass), zero rows of empty sequences, length checks
+    const int et = threadIdx.x - 64, ew = et >> 5;
+    const int per = (p.B + 127) / 128;
+    const int b0 = min(p.B, et * per), b1 = min(p.B, b0 + per);
+    int mine = 0;
+    for (int b = b0; b < b1; ++b) mine += (clamp_len(p, b) + TT - 1) / TT;
+    int inc = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    if (lane == 31) tl->scan[ew] = inc;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    int before = 0;
+    for (int w = 0; w < ew; ++w) before += tl->scan[w];
+    int run = before + inc - mine;
+    for (int b = b0; b < b1; ++b) {
+      tl->prefix[b] = run;
+      if (c == 0) sp.tile_prefix[b] = run;
+      const int raw = p.seq_lens[b];
+      const int L = clamp_len(p, b);
+      if (c == 0 && (raw < 0 || raw > p.max_seq_len)) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+      if (L == 0 && b % grid == c) {
+        uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)b * p.Hq * kD;
+        for (int e = 0; e < p.Hq * kD; ++e) o[e] = 0;
+      }
+      run += (L + TT - 1) / TT;
+    }
+    if (et == 127) {
+      tl->prefix[p.B] = run;
+      if (c == 0) sp.tile_prefix[p.B] = run;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const int T = tl->prefix[p.B];
+  const int t_begin = range_start(c, T, grid), t_end = range_start(c + 1, T, grid);
   const uint32_t tmem = tl->tmem_base;
   const uint32_t ring_addr = smem_addr(smem + Gm::kRingOff);
   const uint32_t q_addr = smem_addr(smem + Gm::kQOff);
@@ -197,7 +250,16 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     int seg_idx = 0;
     bool ok = true;
     int tile = t_begin;
-    int b = t_begin < t_end ? sp.first_seq[c] : 0;
+    int b = 0;
+    if (t_begin < t_end) {        // the sequence holding this CTA's first tile
+      int lo = 0, hi = p.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tl->prefix[mid] <= t_begin) lo = mid;
+        else hi = mid - 1;
+      }
+      b = lo;
+    }
     while (ok) {
       SegInfo sg;
       sg.valid = 0;
@@ -205,8 +267,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (tile < t_end) {
         int tpb1;
         for (;;) {                       // skip sequences without tiles
-          tpb = sp.tile_prefix[b];
-          tpb1 = sp.tile_prefix[b + 1];
+          tpb = tl->prefix[b];
+          tpb1 = tl->prefix[b + 1];
           if (tpb1 > tile) break;
           ++b;
         }
@@ -606,73 +668,6 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
 }
 
-// Tile prefix over the sequences, the first sequence of every CTA's range,
-// zero rows for empty sequences.  One CTA of 1024 threads.
-__global__ void __launch_bounds__(1024)
-plan_sk_kernel(const DecodeParams p, int TT, int grid, int* tile_prefix, int* first_seq,
-               int* total_tiles) {
-  __shared__ int warp_tot[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (p.B + 1023) / 1024;
-  const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
-  int mine = 0;
-  for (int b = b0; b < b1; ++b) {
-    const int raw = p.seq_lens[b];
-    if (raw < 0 || raw > p.max_seq_len) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
-    mine += (clamp_len(p, b) + TT - 1) / TT;
-  }
-  int inc = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int v = warp_tot[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xFFFFFFFFu, v, o);
-      if (lane >= o) v += u;
-    }
-    warp_tot[lane] = v;
-  }
-  __syncthreads();
-  int run = inc - mine + (warp ? warp_tot[warp - 1] : 0);
-  for (int b = b0; b < b1; ++b) {
-    tile_prefix[b] = run;
-    const int L = clamp_len(p, b);
-    run += (L + TT - 1) / TT;
-    if (L == 0) {
-      uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)b * p.Hq * p.D;
-      for (int e = 0; e < p.Hq * p.D; ++e) o[e] = 0;
-    }
-  }
-  const int T = warp_tot[31];
-  if (tid == 0) {
-    tile_prefix[p.B] = T;
-    *total_tiles = T;
-  }
-  __syncthreads();
-  __threadfence_block();
-  // first sequence of each CTA: the b with prefix[b] <= start < prefix[b+1]
-  for (int cc = tid; cc < grid; cc += 1024) {
-    const int start = range_start(cc, T, grid);
-    int lo = 0, hi = p.B - 1;
-    if (T == 0) {
-      first_seq[cc] = 0;
-      continue;
-    }
-    while (lo < hi) {        // last b with tile_prefix[b] <= start
-      const int mid = (lo + hi + 1) >> 1;
-      if (tile_prefix[mid] <= start) lo = mid;
-      else hi = mid - 1;
-    }
-    first_seq[cc] = lo;
-  }
-}
-
 // Merge the partials of sequences cut by CTA range boundaries.  One warp per
 // (sequence, query head).
 template <int DT>
@@ -681,13 +676,14 @@ combine_sk_kernel(const SkParams sp, int grid) {
   const DecodeParams& p = sp.p;
   constexpr int PER = kD / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  wait_prior_grid();           // partials and the tile prefix come from the main kernel
   const int64_t row = (int64_t)blockIdx.x * 4 + warp;
   if (row >= (int64_t)p.B * p.Hq) return;
   const int b = (int)(row / p.Hq), q = (int)(row - (int64_t)b * p.Hq);
-  const int T = *sp.total_tiles;
+  const int T = sp.tile_prefix[p.B];
   const int tpb = sp.tile_prefix[b], tpb1 = sp.tile_prefix[b + 1];
   if (tpb1 <= tpb) return;                                  // empty: zeroed by the plan
-  auto owner = [&](int x) { return (int)(((long long)(x + 1) * grid - 1) / T); };
+  auto owner = [&](int x) { return (int)(((unsigned)(x + 1) * (unsigned)grid - 1u) / (unsigned)T); };
   const int cf = owner(tpb), cl = owner(tpb1 - 1);
   if (cf == cl) return;                                     // written directly
   // CTAs whose range is empty (fewer tiles than CTAs) wrote no partial
@@ -738,6 +734,25 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream finishes; it waits (griddepcontrol.wait)
+// before touching data that kernel produced.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, int smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int device_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -757,8 +772,9 @@ pa_status launch_t(const SkParams& sp, const CUtensorMap& k, const CUtensorMap& 
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   });
   if (attr != cudaSuccess) return PA_ERR_CUDA;
-  decode_tcg_kernel<DT, H, G><<<grid, kThreads, bytes, stream>>>(k, v, q, sp);
-  PA_CHECK_LAUNCH();
+  if (launch_pdl(decode_tcg_kernel<DT, H, G>, grid, kThreads, bytes, stream, k, v, q, sp) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
   return PA_OK;
 }
 
@@ -780,6 +796,7 @@ bool tcg_supported(const DecodeParams& p) {
   const int G = p.Hq / p.Hkv;
   if (p.D != kD) return false;
   if (p.Hkv != 4 && p.Hkv != 8) return false;
+  if (p.B > kMaxSeqs) return false;
   if (G != 1 && G != 2 && G != 4 && G != 8) return false;
   if ((long long)p.num_blocks * p.bs >= (1ll << 31)) return false;
   if ((long long)p.B * p.Hq >= (1ll << 31)) return false;
@@ -790,9 +807,7 @@ SkLayout sk_layout(int B, int Hq) {
   auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
   SkLayout l;
   l.prefix_off = 0;
-  l.first_off = l.prefix_off + a((size_t)(B + 1) * sizeof(int));
-  l.total_off = l.first_off + a((size_t)kSkMaxGrid * sizeof(int));
-  l.m_off = l.total_off + 256;
+  l.m_off = l.prefix_off + a((size_t)(B + 1) * sizeof(int));
   const size_t parts = (size_t)kSkMaxGrid * 2 * Hq;
   l.l_off = l.m_off + a(parts * sizeof(float));
   l.acc_off = l.l_off + a(parts * sizeof(float));
@@ -838,16 +853,10 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
   SkParams sp;
   sp.p = p;
   sp.tile_prefix = reinterpret_cast<int*>(ws + l.prefix_off);
-  sp.first_seq = reinterpret_cast<int*>(ws + l.first_off);
-  sp.total_tiles = reinterpret_cast<int*>(ws + l.total_off);
   sp.part_m = reinterpret_cast<float*>(ws + l.m_off);
   sp.part_l = reinterpret_cast<float*>(ws + l.l_off);
   sp.part_acc = reinterpret_cast<float*>(ws + l.acc_off);
 
-  plan_sk_kernel<<<1, 1024, 0, stream>>>(p, TT, grid, const_cast<int*>(sp.tile_prefix),
-                                         const_cast<int*>(sp.first_seq),
-                                         const_cast<int*>(sp.total_tiles));
-  PA_CHECK_LAUNCH();
   pa_status st;
   if (p.dtype == PA_BFLOAT16)
     st = H == 4 ? launch_h<PA_BFLOAT16, 4>(G, sp, tk, tv, tq, grid, stream)
@@ -858,11 +867,12 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
   if (st != PA_OK) return st;
   const long long rows = (long long)p.B * p.Hq;
   if (rows == 0) return PA_OK;
-  const unsigned cgrid = (unsigned)((rows + 3) / 4);
-  if (p.dtype == PA_BFLOAT16) combine_sk_kernel<PA_BFLOAT16><<<cgrid, 128, 0, stream>>>(sp, grid);
-  else combine_sk_kernel<PA_FLOAT16><<<cgrid, 128, 0, stream>>>(sp, grid);
-  PA_CHECK_LAUNCH();
-  return PA_OK;
+  const int cgrid = (int)((rows + 3) / 4);
+  const cudaError_t e =
+      p.dtype == PA_BFLOAT16
+          ? launch_pdl(combine_sk_kernel<PA_BFLOAT16>, cgrid, 128, 0, stream, sp, grid)
+          : launch_pdl(combine_sk_kernel<PA_FLOAT16>, cgrid, 128, 0, stream, sp, grid);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa

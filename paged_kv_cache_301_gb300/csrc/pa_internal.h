@@ -45,7 +45,7 @@ pa_status launch_decode_tc(const DecodeParams& p, int2* items, int* queue, cudaS
 // (head_dim 128, Hkv 4 or 8, G in {1,2,4,8}): plan + main + combine kernels.
 constexpr int kSkMaxGrid = 160;          // persistent CTAs at most (GB300: 152 SMs)
 struct SkLayout {
-  size_t prefix_off, first_off, total_off, m_off, l_off, acc_off, total;
+  size_t prefix_off, m_off, l_off, acc_off, total;
 };
 SkLayout sk_layout(int B, int Hq);
 bool tcg_supported(const DecodeParams& p);
