@@ -17,6 +17,8 @@ reshape_and_cache_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
                          const int32_t* __restrict__ slot_mapping, int num_tokens,
                          int64_t src_token_vecs, int row_vecs, int64_t num_slots,
                          int32_t* status_dev) {
+  allow_next_grid();
+  wait_prior_grid();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = (int64_t)num_tokens * row_vecs;
   if (i >= total) return;
@@ -39,6 +41,8 @@ __global__ void __launch_bounds__(256)
 copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
                    const int32_t* __restrict__ pairs, int block_vecs, int num_blocks,
                    int32_t* status_dev) {
+  allow_next_grid();
+  wait_prior_grid();
   const int pair = blockIdx.x;
   const int32_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -64,6 +68,8 @@ __global__ void decode_slots_kernel(int32_t* __restrict__ slot_mapping,
                                     const int32_t* __restrict__ block_tables,
                                     const int32_t* __restrict__ seq_lens, int num_seqs,
                                     int max_blocks, int block_size) {
+  allow_next_grid();
+  wait_prior_grid();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= num_seqs) return;
   const int len = seq_lens[b];
@@ -107,10 +113,11 @@ extern "C" pa_status pa_reshape_and_cache(void* k_pool, void* v_pool, const void
   const int64_t total = (int64_t)num_tokens * row_vecs;
   const int64_t grid = (total + 255) / 256;
   if (grid > 0x7FFFFFFF) return PA_ERR_INVALID_ARG;
-  reshape_and_cache_kernel<<<(unsigned)grid, 256, 0, stream>>>(
-      (uint4*)k_pool, (uint4*)v_pool, (const uint4*)key, (const uint4*)value, slot_mapping,
-      num_tokens, stride / 8, row_vecs, (int64_t)num_blocks * block_size, status_dev);
-  PA_CHECK_LAUNCH();
+  if (launch_pdl(reshape_and_cache_kernel, dim3((unsigned)grid), 256, 0, stream, (uint4*)k_pool,
+                 (uint4*)v_pool, (const uint4*)key, (const uint4*)value, slot_mapping, num_tokens,
+                 (int64_t)(stride / 8), row_vecs, (int64_t)num_blocks * block_size,
+                 status_dev) != cudaSuccess)
+    return PA_ERR_CUDA;
   return PA_OK;
 }
 
@@ -125,10 +132,10 @@ extern "C" pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* b
   if (!aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_INVALID_ARG;
   const int64_t block_elems = (int64_t)block_size * num_kv_heads * head_dim;
   if (block_elems / 8 > 0x7FFFFFFF) return PA_ERR_INVALID_ARG;
-  dim3 grid((unsigned)num_pairs, 2);
-  copy_blocks_kernel<<<grid, 256, 0, stream>>>((uint4*)k_pool, (uint4*)v_pool, block_pairs,
-                                               (int)(block_elems / 8), num_blocks, status_dev);
-  PA_CHECK_LAUNCH();
+  if (launch_pdl(copy_blocks_kernel, dim3((unsigned)num_pairs, 2), 256, 0, stream, (uint4*)k_pool,
+                 (uint4*)v_pool, block_pairs, (int)(block_elems / 8), num_blocks,
+                 status_dev) != cudaSuccess)
+    return PA_ERR_CUDA;
   return PA_OK;
 }
 
@@ -138,8 +145,9 @@ extern "C" pa_status pa_decode_slots(int32_t* slot_mapping, const int32_t* block
   if (num_seqs < 0 || max_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   if (!slot_mapping || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
-  decode_slots_kernel<<<(num_seqs + 127) / 128, 128, 0, stream>>>(
-      slot_mapping, block_tables, seq_lens, num_seqs, max_blocks, block_size);
-  PA_CHECK_LAUNCH();
+  if (launch_pdl(decode_slots_kernel, dim3((unsigned)((num_seqs + 127) / 128)), 128, 0, stream,
+                 slot_mapping, block_tables, seq_lens, num_seqs, max_blocks,
+                 block_size) != cudaSuccess)
+    return PA_ERR_CUDA;
   return PA_OK;
 }

@@ -55,6 +55,35 @@ __device__ __forceinline__ void report(int32_t* status_dev, int code) {
   if (status_dev) atomicCAS(status_dev, 0, code);
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may be
+// scheduled before the previous kernel in the stream has finished; it calls
+// wait_prior_grid() before touching data that kernel produces (returns at once
+// when there is no such dependency).  allow_next_grid() lets the next kernel be
+// scheduled early; that kernel still waits for this grid to complete.
+__device__ __forceinline__ void wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_next_grid() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, int threads, int smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 }  // namespace pa
 
 // Map the last launch error to a status code.

@@ -120,18 +120,6 @@ __device__ __forceinline__ int range_start(int c, int T, int grid) {
   return (int)((unsigned)c * (unsigned)T / (unsigned)grid);
 }
 
-// Wait until the kernel this launch depends on (previous in the stream) has
-// completed and its writes are visible; returns at once without such a launch.
-__device__ __forceinline__ void wait_prior_grid() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// Allow the next kernel in the stream (launched with programmatic serialization)
-// to be scheduled; it still waits for this grid to finish before reading.
-__device__ __forceinline__ void allow_next_grid() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 template <int DT, int H, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -231,6 +219,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
   tc_fence_after();
   const int T = tl->prefix[p.B];
   const int t_begin = range_start(c, T, grid), t_end = range_start(c + 1, T, grid);
+  // Ring order follows the MMA's consumption order: K(0), then for t >= 1 K(t)
+  // before V(t-1), and V(last) at the end.  Positions in that sequence:
+  const int t_last = t_end - t_begin - 1;
+  auto pos_k = [](int t) { return t == 0 ? 0 : 2 * t - 1; };
+  auto pos_v = [t_last](int t) { return t < t_last ? 2 * t + 2 : 2 * t + 1; };
   const uint32_t tmem = tl->tmem_base;
   const uint32_t ring_addr = smem_addr(smem + Gm::kRingOff);
   const uint32_t q_addr = smem_addr(smem + Gm::kQOff);
@@ -250,6 +243,34 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     int seg_idx = 0;
     bool ok = true;
     int tile = t_begin;
+    // V tile of the previous K tile, issued after the next K tile
+    bool pend = false;
+    int pend_nops = 0, pend_box = 0, pend_off = 0;
+    int32_t pend_blk = 0;
+    auto issue = [&](const CUtensorMap* map, int nops, int box_tokens, int tok_off,
+                     int32_t blk) -> bool {
+      const uint32_t bytes = (uint32_t)nops * box_tokens * H * 128u * 2u;
+      bool good = true;
+      if (lane == 0) {
+        good = mbar_wait(&tl->empty[stage], sphase ^ 1, abort_flag, kWaitNs);
+        if (good) mbar_arrive_expect_tx(&tl->full[stage], bytes);
+        else set_abort();
+      }
+      good = __shfl_sync(0xFFFFFFFFu, (int)good, 0) != 0;
+      if (!good) return false;
+      if (lane < nops) {
+        uint8_t* dst = smem + Gm::kRingOff + stage * kStage + lane * box_tokens * H * 128;
+        const int row = blk * p.bs + tok_off;
+        tma_load_3d_hint(dst, map, &tl->full[stage], 0, 0, row, policy);
+        tma_load_3d_hint(dst + kSlab, map, &tl->full[stage], 64, 0, row, policy);
+      }
+      issued[stage] = sphase;
+      if (++stage == S) {
+        stage = 0;
+        sphase ^= 1;
+      }
+      return true;
+    };
     int b = 0;
     if (t_begin < t_end) {        // the sequence holding this CTA's first tile
       int lo = 0, hi = p.B - 1;
@@ -279,6 +300,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         sg.direct = (sg.j0 == 0 && sg.j1 == tpb1 - tpb);
         sg.slot = seg_idx == 0 ? 0 : 1;
         sg.valid = 1;
+      }
+      if (!sg.valid && pend) {           // the last V tile of this CTA
+        ok = issue(&tm_v, pend_nops, pend_box, pend_off, pend_blk);
+        pend = false;
+        if (!ok) break;
       }
       const int islot = seg_idx & 1;
       if (lane == 0) {
@@ -342,32 +368,17 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
           cur = nxt;
           nxt = load_chunk(kb + 32);
         }
-        const uint32_t bytes = (uint32_t)nops * box_tokens * H * 128u * 2u;
-        for (int kv = 0; kv < 2 && ok; ++kv) {
-          if (lane == 0) {
-            ok = mbar_wait(&tl->empty[stage], sphase ^ 1, abort_flag, kWaitNs);
-            if (ok) mbar_arrive_expect_tx(&tl->full[stage], bytes);
-            else set_abort();
-          }
-          ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
-          if (!ok) break;
-          const int src = k0 + (lane < nops ? lane : 0) - kb;
-          const int32_t a = __shfl_sync(0xFFFFFFFFu, cur, src & 31);
-          const int32_t bb = __shfl_sync(0xFFFFFFFFu, nxt, src & 31);
-          const int32_t blk = src < 32 ? a : bb;
-          if (lane < nops) {
-            const CUtensorMap* map = kv == 0 ? &tm_k : &tm_v;
-            uint8_t* dst = smem + Gm::kRingOff + stage * kStage + lane * box_tokens * H * 128;
-            const int row = blk * p.bs + tok_off;
-            tma_load_3d_hint(dst, map, &tl->full[stage], 0, 0, row, policy);
-            tma_load_3d_hint(dst + kSlab, map, &tl->full[stage], 64, 0, row, policy);
-          }
-          issued[stage] = sphase;
-          if (++stage == S) {
-            stage = 0;
-            sphase ^= 1;
-          }
-        }
+        const int src = k0 + (lane < nops ? lane : 0) - kb;
+        const int32_t a = __shfl_sync(0xFFFFFFFFu, cur, src & 31);
+        const int32_t bb = __shfl_sync(0xFFFFFFFFu, nxt, src & 31);
+        const int32_t blk = src < 32 ? a : bb;
+        ok = issue(&tm_k, nops, box_tokens, tok_off, blk);
+        if (ok && pend) ok = issue(&tm_v, pend_nops, pend_box, pend_off, pend_blk);
+        pend = true;
+        pend_nops = nops;
+        pend_box = box_tokens;
+        pend_off = tok_off;
+        pend_blk = blk;
       }
       if (!ok) break;
       tile = tpb + sg.j1;
@@ -386,7 +397,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     constexpr uint32_t ab = DT == PA_BFLOAT16 ? 1u : 0u;
     constexpr uint32_t idesc_s = idesc_f16(ab, 0, 0, kRows, N);
     constexpr uint32_t idesc_o = idesc_f16(ab, 1, 0, kD, N);
-    int stage = 0, sphase = 0, tile_g = 0, seg_idx = 0;
+    int tile_g = 0, seg_idx = 0;
     bool ok = true, committed = false;
     auto issue_pv = [&](int t, int vs, int vph) -> bool {
       const int slot = t & 1, ph = (t >> 1) & 1;
@@ -437,10 +448,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int j = 0; j < ntiles && ok; ++j) {
           const int t = tile_g + j;
           const int slot = t & 1, ph = (t >> 1) & 1;
-          const int ks = stage, kph = sphase;
-          if (++stage == S) { stage = 0; sphase ^= 1; }
-          const int vs = stage, vph = sphase;
-          if (++stage == S) { stage = 0; sphase ^= 1; }
+          const int ks = pos_k(t) % S, kph = (pos_k(t) / S) & 1;
+          const int vs = pos_v(t) % S, vph = (pos_v(t) / S) & 1;
           ok = mbar_wait(&tl->full[ks], kph, abort_flag, kWaitNs) &&
                mbar_wait(&tl->s_empty[slot], ph ^ 1, abort_flag, kWaitNs);
           if (!ok) break;
@@ -595,7 +604,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         // rows of tokens past the end: zero their V row (0 * garbage must not reach O)
         if ((sg.j0 + j + 1) * TT > sg.L) {
-          const int u = 2 * t + 1;
+          const int u = pos_v(t);
           const int vs = u % S, vph = (u / S) & 1;
           if (!wait_all(&tl->full[vs], vph)) { ok = false; break; }
           if (!valid) {
@@ -669,7 +678,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
 }
 
 // Merge the partials of sequences cut by CTA range boundaries.  One warp per
-// (sequence, query head).
+// (sequence, query head): lanes read the parts' (max, sum) in parallel, then
+// the accumulators are summed with the per-part weights, loads of all parts in
+// flight together.
 template <int DT>
 __global__ void __launch_bounds__(128)
 combine_sk_kernel(const SkParams sp, int grid) {
@@ -682,37 +693,62 @@ combine_sk_kernel(const SkParams sp, int grid) {
   const int b = (int)(row / p.Hq), q = (int)(row - (int64_t)b * p.Hq);
   const int T = sp.tile_prefix[p.B];
   const int tpb = sp.tile_prefix[b], tpb1 = sp.tile_prefix[b + 1];
-  if (tpb1 <= tpb) return;                                  // empty: zeroed by the plan
+  if (tpb1 <= tpb) return;                                  // empty: zeroed by the main kernel
   auto owner = [&](int x) { return (int)(((unsigned)(x + 1) * (unsigned)grid - 1u) / (unsigned)T); };
   const int cf = owner(tpb), cl = owner(tpb1 - 1);
   if (cf == cl) return;                                     // written directly
-  // CTAs whose range is empty (fewer tiles than CTAs) wrote no partial
-  float M = -CUDART_INF_F;
-  for (int cc = cf + lane; cc <= cl; cc += 32) {
+  const int nparts = cl - cf + 1;
+  // per-lane part: its partial index (or -1 for a CTA whose range is empty)
+  auto part_index = [&](int i) -> int64_t {
+    const int cc = cf + i;
     const int st = range_start(cc, T, grid);
-    if (st == range_start(cc + 1, T, grid)) continue;
+    if (st == range_start(cc + 1, T, grid)) return -1;
     const int slot = st >= tpb ? 0 : 1;
-    M = fmaxf(M, sp.part_m[((int64_t)cc * 2 + slot) * p.Hq + q]);
+    return ((int64_t)cc * 2 + slot) * p.Hq + q;
+  };
+  float M = -CUDART_INF_F;
+  for (int i = lane; i < nparts; i += 32) {
+    const int64_t idx = part_index(i);
+    if (idx >= 0) M = fmaxf(M, sp.part_m[idx]);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-  float den = 0.f, o_acc[PER];
+  float den = 0.f, acc[PER];
 #pragma unroll
-  for (int i = 0; i < PER; ++i) o_acc[i] = 0.f;
-  for (int cc = cf; cc <= cl; ++cc) {
-    const int st = range_start(cc, T, grid);
-    if (st == range_start(cc + 1, T, grid)) continue;
-    const int slot = st >= tpb ? 0 : 1;
-    const int64_t idx = ((int64_t)cc * 2 + slot) * p.Hq + q;
-    const float w = exp2f(sp.part_m[idx] - M);
-    den = fmaf(w, sp.part_l[idx], den);
-#pragma unroll
-    for (int i = 0; i < PER; ++i) o_acc[i] = fmaf(w, sp.part_acc[idx * kD + lane * PER + i], o_acc[i]);
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  for (int base = 0; base < nparts; base += 32) {
+    const int i = base + lane;
+    int64_t idx = -1;
+    float w = 0.f;
+    if (i < nparts) {
+      idx = part_index(i);
+      if (idx >= 0) {
+        w = exp2f(sp.part_m[idx] - M);
+        den = fmaf(w, sp.part_l[idx], den);
+      }
+    }
+    const int cnt = min(32, nparts - base);
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+      const float wk = __shfl_sync(0xFFFFFFFFu, w, k);
+      const long long ik = __shfl_sync(0xFFFFFFFFu, (long long)idx, k);
+      if (ik >= 0) {
+        const float4 v = *reinterpret_cast<const float4*>(sp.part_acc + ik * kD + lane * PER);
+        acc[0] = fmaf(wk, v.x, acc[0]);
+        acc[1] = fmaf(wk, v.y, acc[1]);
+        acc[2] = fmaf(wk, v.z, acc[2]);
+        acc[3] = fmaf(wk, v.w, acc[3]);
+      }
+    }
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
   const float inv = 1.f / den;
   uint16_t* out = static_cast<uint16_t*>(p.out) + row * kD + lane * PER;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) out[i] = narrow<DT>(o_acc[i] * inv);
+  uint2 packed;
+  packed.x = narrow2<DT>(acc[0] * inv, acc[1] * inv);
+  packed.y = narrow2<DT>(acc[2] * inv, acc[3] * inv);
+  *reinterpret_cast<uint2*>(out) = packed;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -734,25 +770,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Launch with programmatic stream serialization: the kernel may be scheduled
-// while the previous kernel in the stream finishes; it waits (griddepcontrol.wait)
-// before touching data that kernel produced.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, int smem,
-                       cudaStream_t stream, Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3((unsigned)threads);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
-
 int device_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -772,8 +789,8 @@ pa_status launch_t(const SkParams& sp, const CUtensorMap& k, const CUtensorMap& 
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   });
   if (attr != cudaSuccess) return PA_ERR_CUDA;
-  if (launch_pdl(decode_tcg_kernel<DT, H, G>, grid, kThreads, bytes, stream, k, v, q, sp) !=
-      cudaSuccess)
+  if (launch_pdl(decode_tcg_kernel<DT, H, G>, dim3((unsigned)grid), kThreads, bytes, stream, k,
+                 v, q, sp) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }
@@ -870,8 +887,8 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
   const int cgrid = (int)((rows + 3) / 4);
   const cudaError_t e =
       p.dtype == PA_BFLOAT16
-          ? launch_pdl(combine_sk_kernel<PA_BFLOAT16>, cgrid, 128, 0, stream, sp, grid)
-          : launch_pdl(combine_sk_kernel<PA_FLOAT16>, cgrid, 128, 0, stream, sp, grid);
+          ? launch_pdl(combine_sk_kernel<PA_BFLOAT16>, dim3((unsigned)cgrid), 128, 0, stream, sp, grid)
+          : launch_pdl(combine_sk_kernel<PA_FLOAT16>, dim3((unsigned)cgrid), 128, 0, stream, sp, grid);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
