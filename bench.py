@@ -157,17 +157,17 @@ def kernel_sources_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name: str):
-    """DRAM bytes per pa_decode launch from the committed ncu summary, if it was
-    taken on the current kernel sources; else None."""
+def recorded_traffic(workload_name: str, kernel: str):
+    """DRAM bytes per launch of the grouped decode kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
-    if not os.path.exists(p):
+    if kernel != "tcg" or not os.path.exists(p):
         return None
     sha = kernel_sources_sha()
     for line in open(p):
         parts = line.split()
         if len(parts) >= 3 and parts[0] == workload_name and parts[1] == sha:
-            return float(parts[2])
+            return int(parts[2])
     return None
 
 
@@ -345,7 +345,7 @@ def run_native(args, dist_info):
     dec_bytes = decode_bytes(step.lens, w, step.max_blocks)
     peak, peak_kind = measured_peaks()
     achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name, step.kernel)
     result = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -396,6 +396,7 @@ def run_native(args, dist_info):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
+            "traffic_unit": "bytes per decode_tcg_kernel launch (ncu dram read + write)",
             "algorithmic_bytes": dec_bytes,
             "avg_launch_ms": round(dec_avg_ms, 5),
         },
