@@ -64,6 +64,23 @@ def decode_bytes(lens, w, max_blocks) -> int:
     return kv_bytes(lens, w) + qo + 4 * blocks + 4 * B
 
 
+def slowest_rank(times_ms, world, device):
+    """Max over ranks of each timing (every rank replicates the workload, so the
+    job takes as long as its slowest rank)."""
+    if world <= 1:
+        return list(times_ms)
+    import torch
+    t = torch.tensor(times_ms, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(bytes_per_rank_step, world, ms_per_step):
+    """Whole-job throughput: the K/V bytes all ranks processed per step over the
+    (slowest-rank) step time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -330,17 +347,14 @@ def run_native(args, dist_info):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
 
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = slowest_rank([total_ms, e2e_ms], world, dev)
     if rank != 0:
         return None
 
     ms_step = total_ms / args.steps
     kvb = kv_bytes(step.lens, w)
     B = len(step.lens)
-    value = world * kvb / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(kvb, world, ms_step)
     dec_avg_ms = sum(decode_ms) / len(decode_ms)
     dec_bytes = decode_bytes(step.lens, w, step.max_blocks)
     peak, peak_kind = measured_peaks()
