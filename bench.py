@@ -205,19 +205,44 @@ class NativeStep:
     def __init__(self, pa, torch, w, dev, partition_tokens: int, kernel: str):
         self.pa, self.torch, self.w, self.dev = pa, torch, w, dev
         bs = w.block_size
-        lens = syn.seq_lens(w)
+        pairs = []
+        if w.length_kind == "shared_prefix":
+            # P prompts, each forked into S samples that share every prompt block
+            # (refcount S); the step appends one token per sample, so each sample
+            # that writes into the shared, partly filled last block first copies
+            # it (copy-on-write), the last holder writes in place.
+            prompt_lens = [w.prefix_tokens + int(k) for k in syn.prompt_extra_tokens(w)]
+            blocks = sum(-(-L // bs) for L in prompt_lens) + w.num_prompts * w.samples_per_prompt
+            nb = int(math.ceil(w.pool_factor * blocks)) + 1
+            bm = pa.BlockManager(nb, bs, syn.shuffled_free_order(nb, syn.rng(w, "free")))
+            pad = bm.allocate(1)[0]
+            seqs = []
+            for L in prompt_lens:
+                root = bm.new_sequence(L)
+                seqs += [root] + [bm.fork(root) for _ in range(w.samples_per_prompt - 1)]
+            for sq in seqs:
+                _, cow = bm.append(sq)
+                if cow is not None:
+                    pairs.append(cow)
+            lens = np.array([bm.seq_len(sq) for sq in seqs], dtype=np.int64)
+            self.unique_tokens = sum(prompt_lens) + len(seqs)
+        else:
+            lens = syn.seq_lens(w)
+            blocks = sum(-(-int(L) // bs) for L in lens)
+            nb = int(math.ceil(w.pool_factor * blocks)) + 1
+            bm = pa.BlockManager(nb, bs, syn.shuffled_free_order(nb, syn.rng(w, "free")))
+            pad = bm.allocate(1)[0]
+            seqs = []
+            for L in lens:
+                s = bm.new_sequence(int(L) - 1)     # context before this step
+                bm.append(s)                        # the step's token: opens a block at a boundary
+                seqs.append(s)
+            self.unique_tokens = int(np.sum(lens))
         B = len(lens)
-        blocks = sum(-(-int(L) // bs) for L in lens)
-        nb = int(math.ceil(w.pool_factor * blocks)) + 1
-        bm = pa.BlockManager(nb, bs, syn.shuffled_free_order(nb, syn.rng(w, "free")))
-        pad = bm.allocate(1)[0]
-        seqs = []
-        for L in lens:
-            s = bm.new_sequence(int(L) - 1)     # context before this step
-            bm.append(s)                        # the step's token: opens a block at a boundary
-            seqs.append(s)
         mb = max(bm.seq_num_blocks(s) for s in seqs)
         tables, seq_lens = bm.export(seqs, mb, pad)
+        self.pairs = (torch.tensor(pairs, dtype=torch.int32, device=dev).reshape(-1, 2)
+                      if pairs else None)
         self.lens = lens
         self.max_blocks = mb
         self.num_blocks = nb
@@ -248,6 +273,8 @@ class NativeStep:
             self.launches_per_step = 2 + 2 + (1 if P > 1 else 0)
         else:                           # main (+ combine)
             self.launches_per_step = 2 + 1 + (1 if P > 1 else 0)
+        if self.pairs is not None:      # copy-on-write block copies
+            self.launches_per_step += 1
         # pinned host copies for the end-to-end measurement
         self.h_q = self.q.cpu().pin_memory()
         self.h_key = self.key.cpu().pin_memory()
@@ -255,12 +282,16 @@ class NativeStep:
         self.h_tables = self.tables.cpu().pin_memory()
         self.h_lens = self.seq_lens.cpu().pin_memory()
         self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h_pairs = self.pairs.cpu().pin_memory() if self.pairs is not None else None
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in
-                             (self.h_q, self.h_key, self.h_value, self.h_tables, self.h_lens))
+                             (self.h_q, self.h_key, self.h_value, self.h_tables, self.h_lens)
+                             + ((self.h_pairs,) if self.h_pairs is not None else ()))
         self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
 
     def write_step(self):
         pa = self.pa
+        if self.pairs is not None:
+            pa.pa_copy_blocks(self.k_pool, self.v_pool, self.pairs)
         pa.pa_decode_slots(self.slots, self.tables, self.seq_lens, self.w.block_size)
         pa.pa_reshape_and_cache(self.k_pool, self.v_pool, self.key, self.value, self.slots)
 
@@ -280,6 +311,8 @@ class NativeStep:
         self.value.copy_(self.h_value, non_blocking=True)
         self.tables.copy_(self.h_tables, non_blocking=True)
         self.seq_lens.copy_(self.h_lens, non_blocking=True)
+        if self.h_pairs is not None:
+            self.pairs.copy_(self.h_pairs, non_blocking=True)
         self.run()
         self.h_out.copy_(self.out, non_blocking=True)
 
@@ -376,8 +409,11 @@ def run_native(args, dist_info):
         "config": {
             "workload": w.name, "num_seqs": B, "num_q_heads": w.num_q_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-            "block_size": w.block_size, "seq_lens": f"{w.length_kind} [{w.lo},{w.hi}]"
-            if w.length_kind != "fixed" else list(w.lens),
+            "block_size": w.block_size, "seq_lens": {
+                "fixed": list(w.lens), "uniform": f"uniform [{w.lo},{w.hi}]",
+                "lognormal": f"lognormal median {w.median:g} sigma {w.sigma:g} clipped [{w.lo},{w.hi}]",
+                "shared_prefix": f"{w.num_prompts} prompts x {w.samples_per_prompt} samples, "
+                                 f"prefix {w.prefix_tokens}+U{{0..{w.prefix_jitter}}}, +1 token"}[w.length_kind],
             "total_tokens": int(np.sum(step.lens)), "num_blocks": step.num_blocks,
             "partition_tokens": args.partition_tokens or 512,
             "kv_bytes_per_step": kvb,
@@ -389,6 +425,9 @@ def run_native(args, dist_info):
                               "simt": "CUDA cores (decode_simt_kernel)"}[step.kernel],
         },
         "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
+        "unique_kv_gbs": round(whole_job_gbs(step.unique_tokens * w.num_kv_heads * w.head_dim * 4,
+                                             world, ms_step), 1),
+        "cow_block_copies_per_step": 0 if step.pairs is None else int(step.pairs.shape[0]),
         "kv_frac_of_peak": round(value / world / peak, 4),
         "wall_s": round(wall, 4),
         "e2e": {
@@ -586,7 +625,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="llama3_8b",
-                    choices=["llama3_8b", "long_context", "ragged", "tiny"])
+                    choices=["llama3_8b", "long_context", "shared_prefix", "ragged", "tiny"])
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_head"], default="auto")
