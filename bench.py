@@ -328,7 +328,7 @@ def run_native(args, dist_info):
     torch.cuda.set_device(dev)
     w = workload(args.workload, args.block_size)
     cpu_baseline = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and w.length_kind != "shared_prefix":
         # before the first GPU call: the oracle's pool is a spawn pool anyway
         cpu_baseline = cpu_oracle_baseline(w, budget_s=args.cpu_budget)
     pa.set_decode_path(args.kernel)
