@@ -1,10 +1,10 @@
 """Benchmark: one decode step of paged attention per timed step, on GB300.
 
-A step is the whole hot path over one batch: the slot of each sequence's newest
-token (pa_decode_slots), the cache write of that token's K/V
-(pa_reshape_and_cache), copy-on-write block copies when the workload shares
-blocks (pa_copy_blocks), and decode attention over the paged pool (pa_decode:
-split-K main kernel + combine).  Inputs are synthetic and seeded; the pool is
+A step is the whole hot path over one batch: copy-on-write block copies when
+the workload shares blocks (pa_copy_blocks), the cache write of each sequence's
+newest token at the slot its block table gives (pa_append_tokens: the slot
+translation and reshape_and_cache in one launch), and decode attention over the
+paged pool (pa_decode: split-K main kernel + combine).  Inputs are synthetic and seeded; the pool is
 resident in HBM before timing starts.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
@@ -267,12 +267,14 @@ class NativeStep:
         # decode_slots + reshape_and_cache + decode (+ plan on the tensor-core
         # path) + combine when a sequence spans several partitions
         self.kernel = decode_kernel_for(w, kernel)
-        if self.kernel == "tcg":      # main + combine
-            self.launches_per_step = 2 + 2
-        elif self.kernel == "tc_head":  # plan + main (+ combine)
-            self.launches_per_step = 2 + 2 + (1 if P > 1 else 0)
-        else:                           # main (+ combine)
-            self.launches_per_step = 2 + 1 + (1 if P > 1 else 0)
+        # append_tokens, then decode: main + combine (grouped), plan + main
+        # (+ combine) (per-head), main (+ combine) (CUDA cores)
+        if self.kernel == "tcg":
+            self.launches_per_step = 1 + 2
+        elif self.kernel == "tc_head":
+            self.launches_per_step = 1 + 2 + (1 if P > 1 else 0)
+        else:
+            self.launches_per_step = 1 + 1 + (1 if P > 1 else 0)
         if self.pairs is not None:      # copy-on-write block copies
             self.launches_per_step += 1
         # pinned host copies for the end-to-end measurement
@@ -292,8 +294,8 @@ class NativeStep:
         pa = self.pa
         if self.pairs is not None:
             pa.pa_copy_blocks(self.k_pool, self.v_pool, self.pairs)
-        pa.pa_decode_slots(self.slots, self.tables, self.seq_lens, self.w.block_size)
-        pa.pa_reshape_and_cache(self.k_pool, self.v_pool, self.key, self.value, self.slots)
+        pa.pa_append_tokens(self.k_pool, self.v_pool, self.key, self.value, self.tables,
+                            self.seq_lens)
 
     def decode(self):
         self.pa.pa_decode(self.out, self.q, self.k_pool, self.v_pool, self.tables, self.seq_lens,
@@ -457,6 +459,102 @@ def run_native(args, dist_info):
         "cpu_baseline": cpu_baseline,
     }
     return result
+
+
+# ----------------------------------------------------------------------------
+# whole-block moves across a model's layers (not the decode step)
+# ----------------------------------------------------------------------------
+
+def run_blocks(args):
+    """--op swap: blocks of every layer's K and V pool between the GPU and pinned
+    CPU memory (pa_swap_blocks, both directions), against a contiguous
+    copy-engine transfer of the same byte count (the link's ceiling).
+    --op cow_layers: copy-on-write clones in every layer's pools in one launch
+    (pa_copy_blocks_multi), against the measured HBM copy peak."""
+    import torch
+    import paged_kv_cache_301_gb300 as pa
+    from paged_kv_cache_301_gb300 import build as _build
+
+    _build.build()
+    torch.cuda.set_device(0)
+    layers, bs, hkv, d = 32, 16, 8, 128            # Llama-3-8B: 32 layers, 8 KV heads
+    pools_n = 2 * layers
+    block_bytes = bs * hkv * d * 2
+    gpu_nb = 1024
+    n = args.pairs
+    g = np.random.default_rng(1234)
+    gpu = [torch.empty((gpu_nb, bs, hkv, d), dtype=torch.bfloat16, device="cuda")
+           for _ in range(pools_n)]
+    for t in gpu:
+        t.normal_()
+    src_ids = g.permutation(gpu_nb)[:n].astype(np.int32)
+    stream = torch.cuda.current_stream()
+
+    def time_it(fn, steps, warmup):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    peak, peak_kind = measured_peaks()
+    moved = n * pools_n * block_bytes
+    if args.op == "swap":
+        cpu_nb = n
+        cpu = [torch.empty((cpu_nb, bs, hkv, d), dtype=torch.bfloat16, pin_memory=True)
+               for _ in range(pools_n)]
+        cpu_ids = g.permutation(cpu_nb).astype(np.int32)
+        out_pairs = torch.from_numpy(np.stack([src_ids, cpu_ids], 1)).cuda()
+        in_pairs = torch.from_numpy(np.stack([cpu_ids, src_ids], 1)).cuda()
+        out_ms = time_it(lambda: pa.pa_swap_blocks(cpu, gpu, out_pairs), args.steps, args.warmup)
+        in_ms = time_it(lambda: pa.pa_swap_blocks(gpu, cpu, in_pairs), args.steps, args.warmup)
+        flat_dev = torch.empty(moved // 2, dtype=torch.bfloat16, device="cuda")
+        flat_host = torch.empty(moved // 2, dtype=torch.bfloat16, pin_memory=True)
+        d2h_ms = time_it(lambda: flat_host.copy_(flat_dev, non_blocking=True), args.steps,
+                         args.warmup)
+        h2d_ms = time_it(lambda: flat_dev.copy_(flat_host, non_blocking=True), args.steps,
+                         args.warmup)
+        gbs = lambda ms: round(moved / (ms * 1e-3) / 1e9, 1)
+        return {
+            "metric": "KV block swap GB/s, GPU pools <-> pinned CPU pools (every layer, one launch)",
+            "value": gbs(out_ms), "unit": "GB/s", "op": "swap", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic N(0,1) pools; seeded block permutation",
+            "config": {"workload": "llama3_8b_layers", "layers": layers, "pools": pools_n,
+                       "block_size": bs, "num_kv_heads": hkv, "head_dim": d,
+                       "block_bytes": block_bytes, "blocks_per_pool": n,
+                       "bytes_per_swap": moved},
+            "swap_out": {"gbs": gbs(out_ms), "ms": round(out_ms, 4),
+                         "frac_of_contiguous_copy": round(d2h_ms / out_ms, 4)},
+            "swap_in": {"gbs": gbs(in_ms), "ms": round(in_ms, 4),
+                        "frac_of_contiguous_copy": round(h2d_ms / in_ms, 4)},
+            "contiguous_copy_engine": {"d2h_gbs": gbs(d2h_ms), "h2d_gbs": gbs(h2d_ms),
+                                       "what": "one cudaMemcpyAsync of the same byte count"},
+            "gpu_launches": 2 * args.steps,
+        }
+    # cow_layers
+    ids = g.permutation(gpu_nb)
+    pairs = torch.from_numpy(np.stack([ids[:n], ids[n:2 * n]], 1).astype(np.int32)).cuda()
+    ms = time_it(lambda: pa.pa_copy_blocks_multi(gpu, pairs), args.steps, args.warmup)
+    gbs = 2 * moved / (ms * 1e-3) / 1e9                # read + write
+    return {
+        "metric": "copy-on-write block copies across all layers, GB/s (read + write)",
+        "value": round(gbs, 1), "unit": "GB/s", "op": "cow_layers", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic N(0,1) pools; seeded block permutation",
+        "config": {"workload": "llama3_8b_layers", "layers": layers, "pools": pools_n,
+                   "block_size": bs, "block_bytes": block_bytes, "pairs": n,
+                   "bytes_copied": moved},
+        "ms": round(ms, 4),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(gbs / peak, 4)},
+        "gpu_launches": args.steps,
+    }
 
 
 # ----------------------------------------------------------------------------
@@ -631,9 +729,21 @@ def main():
     ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_head"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--op", choices=["decode", "swap", "cow_layers"], default="decode",
+                    help="decode: the decode step (default); swap / cow_layers: whole-block "
+                         "moves over a 32-layer model's pools")
+    ap.add_argument("--pairs", type=int, default=512, help="blocks per pool moved (--op swap, "
+                                                           "cow_layers)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.op != "decode":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": args.op,
+                              "unavailable": "no CPU arm for block moves"}), flush=True)
+        else:
+            print(json.dumps(run_blocks(args)), flush=True)
+        return
     dist_info = dist_setup(args)
     if args.impl == "reference":
         res = run_reference(args, dist_info)

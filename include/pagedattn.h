@@ -226,6 +226,66 @@ pa_status pa_decode_slots(int32_t* slot_mapping, const int32_t* block_tables,
                           const int32_t* seq_lens, int num_seqs, int max_blocks,
                           int block_size, cudaStream_t stream);
 
+/*
+ * Decode-step cache write in one launch: pa_decode_slots followed by
+ * pa_reshape_and_cache.  For every sequence b with L = seq_lens[b] > 0, token
+ * L - 1 (the newest, already counted in L) is stored at its pool slot
+ *   slot = block_tables[b][(L-1) / block_size] * block_size + (L-1) % block_size
+ * (tutorial §4 PhysicalIndex): k_pool/v_pool rows of that slot = key[b] / value[b]
+ * ([num_kv_heads, head_dim], token stride kv_token_stride elements, 0 = packed).
+ * slot_mapping (nullable, [num_seqs] int32) receives the slots, -1 for empty
+ * sequences.  A length beyond max_blocks * block_size or a slot outside the pool
+ * is skipped (and reported in checked mode).  Exact bit copies.
+ */
+pa_status pa_append_tokens(void* k_pool, void* v_pool, const void* key, const void* value,
+                           const int32_t* block_tables, const int32_t* seq_lens,
+                           int32_t* slot_mapping, int num_seqs, int64_t kv_token_stride,
+                           int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                           int num_blocks, int dtype, int32_t* status_dev, cudaStream_t stream);
+
+/*
+ * Copy-on-write across a whole model in one launch ("10 — Paged Attention"
+ * tutorial §5 "Copy-on-write sharing"; a model keeps one K and one V pool per
+ * layer, subroutine-cs article §1 bytes-per-token formula).  For every pair
+ * (src, dst) of block_pairs ([num_pairs, 2] int32, device memory) and every
+ * pool i < num_pools: block dst of pools[i] = block src of pools[i].
+ *   pools        host array of num_pools device pointers (the K and V pools of
+ *                every layer, any order), each num_blocks blocks of block_bytes
+ *                bytes (block_size * num_kv_heads * head_dim * element size for
+ *                the [num_blocks, block_size, num_kv_heads, head_dim] layout);
+ *                16-byte aligned; read during the call only.
+ *   block_bytes  a multiple of 16.  num_pools <= 512.
+ * A block id outside [0, num_blocks) skips its pair (reported in checked mode).
+ * A dst that is also a src, or appears twice, is a caller error.  Exact bit
+ * copies.
+ */
+pa_status pa_copy_blocks_multi(void* const* pools, int num_pools, const int32_t* block_pairs,
+                               int num_pairs, int64_t block_bytes, int num_blocks,
+                               int32_t* status_dev, cudaStream_t stream);
+
+/*
+ * Block swap between GPU pools and pools in CPU RAM (the PagedAttention glossary
+ * page, allocation and eviction: blocks of evicted sequences paged to CPU RAM).
+ * For every pair (src, dst) of block_pairs and every pool i < num_pools: block
+ * dst of dst_pools[i] = block src of src_pools[i].  Swap-out passes GPU pools as
+ * src and host pools as dst; swap-in the reverse; GPU-to-GPU also works.
+ *   dst_pools, src_pools  host arrays of num_pools pointers, each to device
+ *                memory or to page-locked host memory (cudaHostAlloc, or
+ *                cudaHostRegister'ed) that the GPU can address; pageable host
+ *                memory is rejected with PA_ERR_INVALID_ARG.  16-byte aligned.
+ *   block_pairs  [num_pairs, 2] int32 (src id, dst id) in device or page-locked
+ *                host memory; src ids index [0, src_num_blocks), dst ids
+ *                [0, dst_num_blocks).
+ *   block_bytes  bytes of one block of one pool, a multiple of 16.
+ * One kernel moves every block of every pool over NVLink-C2C with plain loads and
+ * stores.  Out-of-range ids skip the pair (reported in checked mode).  The host
+ * memory must stay untouched by the CPU until the stream has passed the call.
+ */
+pa_status pa_swap_blocks(void* const* dst_pools, const void* const* src_pools, int num_pools,
+                         const int32_t* block_pairs, int num_pairs, int64_t block_bytes,
+                         int src_num_blocks, int dst_num_blocks, int32_t* status_dev,
+                         cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Host block manager                                                        */
 /* ------------------------------------------------------------------------ */

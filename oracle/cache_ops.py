@@ -12,7 +12,16 @@ sharing"; subroutine-cs article §3 "Copy-on-Write and Parallel Sampling").  Eve
 slot of the source block (all bs rows, all KV heads) is copied to the
 destination block, for keys and for values.
 
-Both work on raw uint16 storage bits, so results are exact bit copies.
+copy_blocks_multi: the same clone in every pool a model keeps, one K and one V
+pool per layer (subroutine-cs article §1, the bytes-per-token formula counts
+2 x layers x heads x head_dim elements per token).
+
+swap_blocks: blocks moved between two sets of pools, e.g. from the GPU pools to
+pools in CPU RAM and back (PagedAttention glossary page, allocation and eviction:
+blocks can be paged to CPU RAM).  Block dst of the destination pool i receives
+block src of the source pool i.
+
+All work on raw uint16 storage bits, so results are exact bit copies.
 """
 from __future__ import annotations
 
@@ -38,3 +47,24 @@ def copy_blocks(k_pool: np.ndarray, v_pool: np.ndarray, pairs) -> None:
     for src, dst in np.asarray(pairs, dtype=np.int64).reshape(-1, 2).tolist():
         k_pool[dst] = k_pool[src]
         v_pool[dst] = v_pool[src]
+
+
+def copy_blocks_multi(pools, pairs) -> None:
+    """In place.  pools: sequence of [NB, ...] arrays (K and V of every layer);
+    every (src, dst) pair is applied, in order, to every pool."""
+    pairs = np.asarray(pairs, dtype=np.int64).reshape(-1, 2).tolist()
+    for pool in pools:
+        for src, dst in pairs:
+            pool[dst] = pool[src]
+
+
+def swap_blocks(dst_pools, src_pools, pairs) -> None:
+    """In place on dst_pools.  pairs: (src id in src_pools, dst id in dst_pools)."""
+    if len(dst_pools) != len(src_pools):
+        raise ValueError("one destination pool per source pool")
+    pairs = np.asarray(pairs, dtype=np.int64).reshape(-1, 2).tolist()
+    for dst_pool, src_pool in zip(dst_pools, src_pools):
+        if dst_pool.shape[1:] != src_pool.shape[1:]:
+            raise ValueError("source and destination blocks differ in shape")
+        for src, dst in pairs:
+            dst_pool[dst] = src_pool[src]

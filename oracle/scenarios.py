@@ -21,6 +21,10 @@ ragged_steps   continuous-batching steps ("PagedAttention" glossary entry,
                each step appends one token per sequence (a fresh block at a
                block boundary, tutorial §4 AppendToken), writes it, then the
                batch decodes with the grown lengths.
+swap_round_trip  some sequences of a batch are evicted to a pool in CPU RAM
+               (PagedAttention glossary entry, allocation and eviction: blocks
+               paged to CPU RAM), other work takes their GPU blocks, and the
+               sequences come back into freshly allocated GPU blocks.
 
 Readings (listed in the design notes): the decode after a write attends to the
 token just written; the shared-prefix fork point is prefix + k_p with
@@ -30,6 +34,7 @@ ascending index, so the last holder of a shared block writes in place.
 """
 from __future__ import annotations
 
+import copy
 import dataclasses
 import math
 from typing import List, Optional
@@ -38,7 +43,7 @@ import numpy as np
 
 import synthetic as syn
 from .block_manager import BlockManager, Sequence, check_invariants
-from .cache_ops import copy_blocks, reshape_and_cache
+from .cache_ops import copy_blocks, reshape_and_cache, swap_blocks
 
 
 @dataclasses.dataclass
@@ -244,3 +249,67 @@ def decode_f64(batch: PagedBatch, sequences=None, heads=None) -> np.ndarray:
     return paged_decode_attention(
         batch.q, batch.k_pool, batch.v_pool, batch.block_tables, batch.seq_lens,
         batch.scale, sequences=sequences, heads=heads, dtype=batch.dtype)
+
+
+@dataclasses.dataclass
+class SwapRoundTrip:
+    before: PagedBatch           # the batch as given (not modified)
+    after: PagedBatch            # after swap-out, reuse of the freed blocks, swap-in
+    cpu_num_blocks: int
+    out_pairs: np.ndarray        # [n, 2] (GPU block, CPU block)
+    in_pairs: np.ndarray         # [n, 2] (CPU block, new GPU block)
+    reused_blocks: np.ndarray    # GPU blocks another sequence took meanwhile (poisoned)
+    cpu_k_pool: np.ndarray       # CPU pools right after the swap-out
+    cpu_v_pool: np.ndarray
+
+
+def swap_round_trip(batch: PagedBatch, swapped, cpu_num_blocks: int,
+                    seed: int = 0) -> SwapRoundTrip:
+    """Evict the sequences `swapped` to CPU pools, let another sequence take (and
+    overwrite) the GPU blocks they freed, then bring them back.
+
+    Swap-out: each evicted sequence gets CPU blocks from a CPU-side block manager
+    (seeded free order), its blocks move GPU -> CPU, its GPU blocks are freed.
+    Reuse: one new sequence allocates exactly the freed blocks (the free stack is
+    last-in first-out) and fills them with NaN.  Swap-in: each evicted sequence
+    allocates new GPU blocks, its blocks move CPU -> GPU, its CPU blocks are freed
+    and its table points at the new blocks.  Attention over the result must be
+    identical to attention over the batch as given."""
+    after = copy.deepcopy(batch)
+    mgr, seqs, bs = after.manager, after.sequences, after.block_size
+    shape = after.k_pool.shape[1:]
+    nan = syn.NAN_BITS[after.dtype]
+    cpu_k = np.full((cpu_num_blocks,) + shape, nan, dtype=np.uint16)
+    cpu_v = cpu_k.copy()
+    cpu_mgr = BlockManager(cpu_num_blocks, bs,
+                           syn.shuffled_free_order(cpu_num_blocks, np.random.default_rng(seed)))
+    out_pairs, cpu_ids = [], {}
+    for b in swapped:
+        ids = cpu_mgr.allocate(len(seqs[b].block_table))
+        cpu_ids[b] = ids
+        out_pairs += list(zip(seqs[b].block_table, ids))
+    out_arr = np.asarray(out_pairs, dtype=np.int32).reshape(-1, 2)
+    swap_blocks([cpu_k, cpu_v], [after.k_pool, after.v_pool], out_arr)
+    cpu_k_out, cpu_v_out = cpu_k.copy(), cpu_v.copy()
+    freed = 0
+    for b in swapped:
+        freed += len(seqs[b].block_table)
+        mgr.free_blocks(seqs[b].block_table)
+        seqs[b].block_table = []
+    reused = mgr.allocate(freed)
+    after.k_pool[reused] = nan
+    after.v_pool[reused] = nan
+    in_pairs = []
+    for b in swapped:
+        new = mgr.allocate(len(cpu_ids[b]))
+        in_pairs += list(zip(cpu_ids[b], new))
+        seqs[b].block_table = new
+    in_arr = np.asarray(in_pairs, dtype=np.int32).reshape(-1, 2)
+    swap_blocks([after.k_pool, after.v_pool], [cpu_k, cpu_v], in_arr)
+    for b in swapped:
+        cpu_mgr.free_blocks(cpu_ids[b])
+    check_invariants(mgr, [[after.pad_block], reused] + [s.block_table for s in seqs])
+    check_invariants(cpu_mgr, [])
+    after.block_tables = _tables(seqs, after.pad_block, batch.max_blocks)
+    return SwapRoundTrip(batch, after, cpu_num_blocks, out_arr, in_arr,
+                         np.asarray(reused, dtype=np.int32), cpu_k_out, cpu_v_out)

@@ -156,6 +156,53 @@ def pa_copy_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, block_pairs: torc
     _check(st, "pa_copy_blocks")
 
 
+def _pool_array(pools: Sequence[torch.Tensor], what: str):
+    """(ctypes array of the pools' addresses, blocks per pool, bytes per block)."""
+    if not pools:
+        raise ValueError(f"{what}: no pools")
+    first = pools[0]
+    for t in pools:
+        if t.shape != first.shape or t.dtype != first.dtype:
+            raise ValueError(f"{what}: every pool needs the same shape and dtype")
+    arr = (ctypes.c_void_p * len(pools))(*[_ptr(t) for t in pools])
+    nb = first.shape[0]
+    return arr, nb, first[0].numel() * first.element_size()
+
+
+def pa_copy_blocks_multi(pools: Sequence[torch.Tensor], block_pairs: torch.Tensor,
+                         status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Copy-on-write clones in every pool (the K and V pools of all layers) in
+    one launch; block_pairs [n, 2] int32 (src, dst) on the device."""
+    arr, nb, block_bytes = _pool_array(pools, "pa_copy_blocks_multi")
+    n = block_pairs.shape[0] if block_pairs.numel() else 0
+    st = lib().pa_copy_blocks_multi(
+        ctypes.cast(arr, ctypes.c_void_p), len(pools), _ptr(block_pairs) if n else None, n,
+        block_bytes, nb, _ptr(status), _stream(stream))
+    _check(st, "pa_copy_blocks_multi")
+
+
+def pa_swap_blocks(dst_pools: Sequence[torch.Tensor], src_pools: Sequence[torch.Tensor],
+                   block_pairs: torch.Tensor, status: Optional[torch.Tensor] = None,
+                   stream=None) -> None:
+    """Block dst of dst_pools[i] = block src of src_pools[i] for every (src, dst)
+    pair and pool.  Pools live on the GPU or in pinned CPU memory
+    (tensor.pin_memory()); block_pairs [n, 2] int32, on the GPU or pinned."""
+    if len(dst_pools) != len(src_pools):
+        raise ValueError("pa_swap_blocks: one destination pool per source pool")
+    darr, dnb, dbytes = _pool_array(dst_pools, "pa_swap_blocks")
+    sarr, snb, sbytes = _pool_array(src_pools, "pa_swap_blocks")
+    if dbytes != sbytes or dst_pools[0].dtype != src_pools[0].dtype:
+        raise ValueError("pa_swap_blocks: source and destination blocks differ")
+    for t in list(dst_pools) + list(src_pools) + [block_pairs]:
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("pa_swap_blocks: CPU tensors must be pinned")
+    n = block_pairs.shape[0] if block_pairs.numel() else 0
+    st = lib().pa_swap_blocks(
+        ctypes.cast(darr, ctypes.c_void_p), ctypes.cast(sarr, ctypes.c_void_p), len(dst_pools),
+        _ptr(block_pairs) if n else None, n, dbytes, snb, dnb, _ptr(status), _stream(stream))
+    _check(st, "pa_swap_blocks")
+
+
 def pa_decode_slots(slot_mapping: torch.Tensor, block_tables: torch.Tensor,
                     seq_lens: torch.Tensor, block_size: int, stream=None) -> torch.Tensor:
     """slot_mapping[b] = pool slot of token seq_lens[b] - 1 (or -1 for empty)."""
@@ -164,6 +211,21 @@ def pa_decode_slots(slot_mapping: torch.Tensor, block_tables: torch.Tensor,
                                block_size, _stream(stream))
     _check(st, "pa_decode_slots")
     return slot_mapping
+
+
+def pa_append_tokens(k_pool: torch.Tensor, v_pool: torch.Tensor, key: torch.Tensor,
+                     value: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                     slot_mapping: Optional[torch.Tensor] = None,
+                     status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Decode-step cache write: the newest token of every sequence (key/value
+    [B, Hkv, D]) goes to its slot, computed from block_tables and seq_lens."""
+    NB, bs, Hkv, D = k_pool.shape
+    B, MB = block_tables.shape
+    st = lib().pa_append_tokens(
+        _ptr(k_pool), _ptr(v_pool), _ptr(key), _ptr(value), _ptr(block_tables), _ptr(seq_lens),
+        _ptr(slot_mapping), B, 0, Hkv, D, bs, MB, NB, _dtype(k_pool), _ptr(status),
+        _stream(stream))
+    _check(st, "pa_append_tokens")
 
 
 class BlockManager:
@@ -250,6 +312,7 @@ class BlockManager:
 __all__ = [
     "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_workspace_bytes",
     "pa_decode_noalloc", "set_decode_path",
-    "alloc_workspace", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_slots",
+    "alloc_workspace", "pa_reshape_and_cache", "pa_append_tokens",
+    "pa_copy_blocks_multi", "pa_swap_blocks", "pa_copy_blocks", "pa_decode_slots",
     "BlockManager", "lib",
 ]

@@ -34,6 +34,13 @@ SIGNATURES = {
     "pa_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_void_p, c_void_p]),
     "pa_set_decode_path": (c_int, [c_int]),
+    "pa_copy_blocks_multi": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int64, c_int, c_void_p,
+                                     c_void_p]),
+    "pa_swap_blocks": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int64, c_int, c_int,
+                               c_void_p, c_void_p]),
+    "pa_append_tokens": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                 c_void_p, c_int, c_int64, c_int, c_int, c_int, c_int, c_int,
+                                 c_int, c_void_p, c_void_p]),
     "pa_decode_slots": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p]),
     "pa_bm_create": (c_int, [c_int, c_int, c_void_p, ctypes.POINTER(c_void_p)]),
     "pa_bm_destroy": (None, [c_void_p]),

@@ -27,7 +27,7 @@ SOURCES = [
     "pa_block_manager.cpp",
     "pa_decode_noalloc.cu",
     "pa_decode_tc.cu",
-    "pa_decode_tcg.cu",
+    "pa_decode_tcg.cu", "pa_blocks.cu",
 ]
 HEADERS = [
     os.path.join(ROOT, "include", "pagedattn.h"),

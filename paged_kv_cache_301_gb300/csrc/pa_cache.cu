@@ -82,6 +82,42 @@ __global__ void decode_slots_kernel(int32_t* __restrict__ slot_mapping,
   slot_mapping[b] = blk * block_size + pos % block_size;
 }
 
+// Newest token of each sequence: slot from the block table, then the copy.
+// One thread per 16-byte vector of one sequence's K (and V) row.
+__global__ void __launch_bounds__(256)
+append_tokens_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                     const uint4* __restrict__ key, const uint4* __restrict__ value,
+                     const int32_t* __restrict__ block_tables,
+                     const int32_t* __restrict__ seq_lens, int32_t* __restrict__ slot_mapping,
+                     int num_seqs, int64_t src_token_vecs, int row_vecs, int block_size,
+                     int max_blocks, int64_t num_slots, int32_t* status_dev) {
+  allow_next_grid();
+  wait_prior_grid();
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)num_seqs * row_vecs) return;
+  const int b = (int)(i / row_vecs);
+  const int v = (int)(i - (int64_t)b * row_vecs);
+  const int L = seq_lens[b];
+  int64_t slot = -1;
+  if (L > 0 && L <= max_blocks * block_size) {
+    const int pos = L - 1;
+    slot = (int64_t)block_tables[(int64_t)b * max_blocks + pos / block_size] * block_size +
+           pos % block_size;
+    if (slot < 0 || slot >= num_slots) {
+      if (v == 0) report(status_dev, PA_ERR_BAD_BLOCK_ID);
+      slot = -1;
+    }
+  } else if (L != 0 && v == 0) {
+    report(status_dev, PA_ERR_BAD_BLOCK_ID);
+  }
+  if (slot_mapping && v == 0) slot_mapping[b] = (int32_t)slot;
+  if (slot < 0) return;
+  const int64_t src = (int64_t)b * src_token_vecs + v;
+  const int64_t dst = slot * row_vecs + v;
+  k_pool[dst] = key[src];
+  v_pool[dst] = value[src];
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -148,6 +184,35 @@ extern "C" pa_status pa_decode_slots(int32_t* slot_mapping, const int32_t* block
   if (launch_pdl(decode_slots_kernel, dim3((unsigned)((num_seqs + 127) / 128)), 128, 0, stream,
                  slot_mapping, block_tables, seq_lens, num_seqs, max_blocks,
                  block_size) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+extern "C" pa_status pa_append_tokens(void* k_pool, void* v_pool, const void* key,
+                                      const void* value, const int32_t* block_tables,
+                                      const int32_t* seq_lens, int32_t* slot_mapping,
+                                      int num_seqs, int64_t kv_token_stride, int num_kv_heads,
+                                      int head_dim, int block_size, int max_blocks,
+                                      int num_blocks, int dtype, int32_t* status_dev,
+                                      cudaStream_t stream) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!supported_shape(head_dim, block_size, dtype)) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (!k_pool || !v_pool || !key || !value || !block_tables || !seq_lens)
+    return PA_ERR_INVALID_ARG;
+  const int64_t row_elems = (int64_t)num_kv_heads * head_dim;
+  const int64_t stride = kv_token_stride == 0 ? row_elems : kv_token_stride;
+  if (stride < row_elems || (stride % 8) != 0) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(key) || !aligned16(value))
+    return PA_ERR_INVALID_ARG;
+  const int row_vecs = (int)(row_elems / 8);
+  const int64_t grid = ((int64_t)num_seqs * row_vecs + 255) / 256;
+  if (grid > 0x7FFFFFFF) return PA_ERR_INVALID_ARG;
+  if (launch_pdl(append_tokens_kernel, dim3((unsigned)grid), 256, 0, stream, (uint4*)k_pool,
+                 (uint4*)v_pool, (const uint4*)key, (const uint4*)value, block_tables, seq_lens,
+                 slot_mapping, num_seqs, (int64_t)(stride / 8), row_vecs, block_size, max_blocks,
+                 (int64_t)num_blocks * block_size, status_dev) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }

@@ -110,6 +110,28 @@ def test_decode_slots_match_block_manager(pa):
     assert (out.cpu().numpy()[:5] == -1).all()
 
 
+@pytest.mark.parametrize("bs", [8, 16, 64])
+def test_append_tokens_matches_slots_then_write(pa, bs):
+    """The fused decode-step write equals decode_slots + reshape_and_cache: same
+    slots as the block manager, bit-exact pools, empty sequences skipped."""
+    initial, steps, final = scenarios.ragged_steps(syn.RAGGED, bs, 2, num_seqs=48)
+    dev = DeviceBatch(initial)
+    dt = syn.RAGGED.dtype
+    k_ref, v_ref = initial.k_pool.copy(), initial.v_pool.copy()
+    for st in steps:
+        lens = st.seq_lens.copy()
+        lens[5] = 0                                   # an empty sequence writes nothing
+        slots = torch.full((len(lens),), 7, dtype=torch.int32, device="cuda")
+        pa.pa_append_tokens(dev.k_pool, dev.v_pool, to_dev(st.key, dt), to_dev(st.value, dt),
+                            i32(st.block_tables), i32(lens), slot_mapping=slots)
+        want = st.slot_mapping.copy()
+        want[5] = -1
+        assert np.array_equal(slots.cpu().numpy(), want)
+        reshape_and_cache(k_ref, v_ref, st.key, st.value, want)
+    torch.cuda.synchronize()
+    _pools_equal(dev, k_ref, v_ref)
+
+
 def test_shared_prefix_workload(pa):
     """16 prompts x 8 forked samples: every step's CoW copies then the new tokens,
     replayed on the GPU; pools bit-exact, then decode against the oracle."""

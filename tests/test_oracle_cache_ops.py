@@ -1,10 +1,12 @@
 """Pins of the oracle's cache write, block copy and copy-on-write flows (CPU only)."""
+import dataclasses
+
 import numpy as np
 
 import synthetic as syn
 from oracle import scenarios
 from oracle.block_manager import BlockManager, Sequence
-from oracle.cache_ops import copy_blocks, reshape_and_cache
+from oracle.cache_ops import copy_blocks, copy_blocks_multi, reshape_and_cache, swap_blocks
 
 
 def _pool(nb, bs, H, D, fill):
@@ -110,3 +112,59 @@ def test_copy_on_write_fires_once_per_sharer():
     got = sum(len(st.cow_pairs) for st in steps)
     # sharers that append copy; the last remaining holder writes in place
     assert got == expect
+
+
+def test_copy_blocks_multi_is_copy_blocks_on_every_layer():
+    """Every layer's K and V pools get the same clones, and nothing else moves;
+    checked element by element against the pools as they were."""
+    g = np.random.default_rng(3)
+    L, NB = 3, 9
+    pools = [g.integers(0, 2**16, size=(NB, 2, 2, 4), dtype=np.uint16) for _ in range(2 * L)]
+    before = [p.copy() for p in pools]
+    pairs = [(4, 0), (7, 2), (1, 8)]
+    copy_blocks_multi(pools, pairs)
+    dst_of = {d: s for s, d in pairs}
+    for p, p0 in zip(pools, before):
+        for blk in range(NB):
+            src = dst_of.get(blk, blk)
+            for idx in np.ndindex(p.shape[1:]):
+                assert p[(blk,) + idx] == p0[(src,) + idx]
+    # one layer through the two-pool copy gives the same bytes
+    k, v = before[0].copy(), before[1].copy()
+    copy_blocks(k, v, pairs)
+    assert np.array_equal(k, pools[0]) and np.array_equal(v, pools[1])
+
+
+def test_swap_blocks_between_pools_of_different_sizes():
+    g = np.random.default_rng(4)
+    gpu = [g.integers(0, 2**16, size=(10, 4, 1, 8), dtype=np.uint16) for _ in range(2)]
+    cpu = [np.zeros((3, 4, 1, 8), dtype=np.uint16) for _ in range(2)]
+    swap_blocks(cpu, gpu, [(9, 0), (2, 2)])
+    for c, gp in zip(cpu, gpu):
+        assert np.array_equal(c[0], gp[9]) and np.array_equal(c[2], gp[2])
+        assert not c[1].any()
+
+
+def test_swap_round_trip_restores_attention_exactly():
+    """Evict half the sequences to CPU RAM, let other work overwrite their GPU
+    blocks, swap them back into different blocks: the fp64 attention is
+    bit-identical (it depends on the logical token order only), the moved blocks
+    hold the same bytes, and the freed blocks were really reused."""
+    w = dataclasses.replace(syn.TINY, pool_factor=3.0)
+    batch = scenarios.fixed_batch(w)
+    want = scenarios.decode_f64(batch)
+    rt = scenarios.swap_round_trip(batch, [0, 2], cpu_num_blocks=16, seed=5)
+    got = scenarios.decode_f64(rt.after)
+    assert np.array_equal(got, want)
+    old = {int(gp): int(c) for gp, c in rt.out_pairs}
+    new = {int(c): int(gp) for c, gp in rt.in_pairs}
+    assert set(old.values()) == set(new)
+    for gp, c in old.items():
+        assert np.array_equal(rt.cpu_k_pool[c], batch.k_pool[gp])
+        assert np.array_equal(rt.after.k_pool[new[c]], batch.k_pool[gp])
+        assert np.array_equal(rt.after.v_pool[new[c]], batch.v_pool[gp])
+    assert set(rt.reused_blocks.tolist()) == set(old)
+    assert not set(new.values()) & set(old)        # the sequences moved
+    assert np.array_equal(rt.before.k_pool, batch.k_pool)
+    # a sequence that was not swapped kept its table
+    assert np.array_equal(rt.after.block_tables[1], batch.block_tables[1])
