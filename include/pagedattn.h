@@ -307,6 +307,8 @@ pa_status pa_bm_create(int num_blocks, int block_size, const int32_t* initial_fr
                        pa_block_manager** out);
 void pa_bm_destroy(pa_block_manager* bm);
 int pa_bm_num_free(const pa_block_manager* bm);
+/* Cached blocks with refcount 0 waiting for eviction (not on the free stack). */
+int pa_bm_num_evictable(const pa_block_manager* bm);
 /* Refcount of a block id (0 when free, -1 when out of range). */
 int pa_bm_refcount(const pa_block_manager* bm, int block_id);
 pa_status pa_bm_allocate(pa_block_manager* bm, int n, int32_t* out_ids);
@@ -322,6 +324,24 @@ pa_status pa_bm_seq_release(pa_block_manager* bm, int seq_id);
 pa_status pa_bm_seq_append(pa_block_manager* bm, int seq_id, int32_t* slot,
                            int32_t* cow_src, int32_t* cow_dst);
 int pa_bm_seq_len(const pa_block_manager* bm, int seq_id);
+/*
+ * Prefix cache ("10 — Paged Attention" tutorial §5, the relationship to prefix
+ * caching): create a sequence holding token_ids[0 .. num_tokens).  Full block i
+ * is keyed by key_i = FNV-1a-64(key_{i-1} as 8 little-endian bytes, then the
+ * block's token ids as 4 little-endian bytes each), key_{-1} = 0, so a key
+ * names the whole prefix.  The leading blocks whose keys (and stored parent key
+ * and token ids) are cached are shared (refcount + 1, or taken off the
+ * eviction queue with refcount 1), up to the first miss; the rest are allocated
+ * and their full blocks registered.  *cached_tokens = tokens whose KV is
+ * already in the pool (a multiple of block_size); the caller computes the KV of
+ * the others before anything reads them.  A cached block whose refcount drops to
+ * zero waits on an eviction queue (blocks of one release last block first) and
+ * is evicted, front first, only when an allocation finds the free stack short.
+ * PA_ERR_OUT_OF_BLOCKS (state unchanged) when free + evictable blocks, minus
+ * the queued blocks this call revives, cannot cover the new blocks.
+ */
+pa_status pa_bm_seq_create_cached(pa_block_manager* bm, const int32_t* token_ids,
+                                  int num_tokens, int* seq_id, int* cached_tokens);
 int pa_bm_seq_num_blocks(const pa_block_manager* bm, int seq_id);
 /* Copy sequence tables into a [n, max_blocks] int32 array (padding with pad_id)
  * and their lengths into seq_lens[n]; fails if a table is longer than max_blocks. */

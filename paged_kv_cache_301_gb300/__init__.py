@@ -255,6 +255,11 @@ class BlockManager:
     def num_free(self) -> int:
         return self._lib.pa_bm_num_free(self._h)
 
+    @property
+    def num_evictable(self) -> int:
+        """Cached blocks with refcount 0 waiting for eviction."""
+        return self._lib.pa_bm_num_evictable(self._h)
+
     def refcount(self, block: int) -> int:
         return self._lib.pa_bm_refcount(self._h, block)
 
@@ -276,6 +281,17 @@ class BlockManager:
         _check(self._lib.pa_bm_seq_create(self._h, prompt_len, ctypes.byref(sid)),
                "pa_bm_seq_create")
         return sid.value
+
+    def new_sequence_cached(self, token_ids: Sequence[int]):
+        """Sequence holding token_ids, sharing the longest cached prefix of full
+        blocks.  Returns (sequence id, tokens whose KV is already cached)."""
+        n = len(token_ids)
+        arr = (ctypes.c_int32 * max(n, 1))(*[int(t) for t in token_ids])
+        sid, cached = ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.pa_bm_seq_create_cached(self._h, arr, n, ctypes.byref(sid),
+                                                 ctypes.byref(cached)),
+               "pa_bm_seq_create_cached")
+        return sid.value, cached.value
 
     def fork(self, seq: int) -> int:
         sid = ctypes.c_int()

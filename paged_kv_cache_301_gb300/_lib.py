@@ -45,6 +45,9 @@ SIGNATURES = {
     "pa_bm_create": (c_int, [c_int, c_int, c_void_p, ctypes.POINTER(c_void_p)]),
     "pa_bm_destroy": (None, [c_void_p]),
     "pa_bm_num_free": (c_int, [c_void_p]),
+    "pa_bm_num_evictable": (c_int, [c_void_p]),
+    "pa_bm_seq_create_cached": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(c_int),
+                                        ctypes.POINTER(c_int)]),
     "pa_bm_refcount": (c_int, [c_void_p, c_int]),
     "pa_bm_allocate": (c_int, [c_void_p, c_int, c_void_p]),
     "pa_bm_free": (c_int, [c_void_p, c_void_p, c_int]),

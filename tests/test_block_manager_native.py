@@ -104,3 +104,63 @@ def test_random_operations_match_oracle(native, seed):
     for row, L, i in zip(tables.tolist(), lens.tolist(), ids):
         t = live[i].block_table
         assert row[:len(t)] == t and L == live[i].length
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prefix_cache_matches_oracle(native, seed):
+    """Random traffic of cached prompts (drawn from a few shared prefixes, so
+    that hits, revivals from the eviction queue and evictions all happen),
+    releases, appends and forks: the native manager hands out the same blocks,
+    reports the same cached prefixes and ends in the same state."""
+    from oracle.prefix_cache import PrefixCachingBlockManager
+    g = np.random.default_rng(100 + seed)
+    nb, bs = 80, [2, 4, 8, 16][seed]
+    order = [int(x) for x in g.permutation(nb)]
+    ob = PrefixCachingBlockManager(nb, bs, order)
+    nbm = native.BlockManager(nb, bs, order)
+    prompts = [list(g.integers(-5, 40, size=int(g.integers(1, 5 * bs)))) for _ in range(5)]
+    live = {}
+    hits = 0
+    for step in range(3000):
+        op = g.integers(0, 6)
+        if op <= 1 or not live:
+            base = prompts[int(g.integers(0, len(prompts)))]
+            toks = base[:int(g.integers(0, len(base) + 1))] + \
+                list(g.integers(-5, 40, size=int(g.integers(0, 2 * bs))))
+            try:
+                o, c = ob.create_sequence(toks)
+            except OutOfBlocks:
+                with pytest.raises(native.PagedAttnError):
+                    nbm.new_sequence_cached(toks)
+                continue
+            sid, nc = nbm.new_sequence_cached(toks)
+            assert nc == c
+            hits += c > 0
+            live[sid] = o
+        elif op == 2:
+            sid = list(live)[int(g.integers(0, len(live)))]
+            live.pop(sid).release()
+            nbm.release(sid)
+        elif op == 3:
+            sid = list(live)[int(g.integers(0, len(live)))]
+            live[nbm.fork(sid)] = live[sid].fork()
+        else:
+            sid = list(live)[int(g.integers(0, len(live)))]
+            try:
+                want = live[sid].append_token()
+            except OutOfBlocks:
+                with pytest.raises(native.PagedAttnError):
+                    nbm.append(sid)
+                continue
+            assert nbm.append(sid) == want
+        assert nbm.num_free == ob.num_free and nbm.num_evictable == ob.num_evictable
+    assert hits > 10
+    for b in range(nb):
+        assert nbm.refcount(b) == ob.refcount.get(b, 0)
+    if live:
+        ids = list(live)
+        mb = max(1, max(len(live[i].block_table) for i in ids))
+        tables, lens = nbm.export(ids, mb, -1)
+        for row, L, i in zip(tables.tolist(), lens.tolist(), ids):
+            t = live[i].block_table
+            assert row[:len(t)] == t and L == live[i].length
