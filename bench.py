@@ -557,6 +557,67 @@ def run_blocks(args):
     }
 
 
+def run_allocsim(args):
+    """--op allocsim: contiguous vs paged KV allocation on a saturated serving
+    stream (Poisson arrivals, lognormal lengths), block-size sweep; host code
+    (pa_sim_run), the oracle's simulator timed beside it."""
+    import paged_kv_cache_301_gb300 as pa
+    from paged_kv_cache_301_gb300 import build as _build
+
+    _build.build()
+    s = syn.SERVING_STREAM
+    a, p, o = syn.request_arrays(s)
+    cap = 26777 * 16
+    runs = [("contiguous", r, 16) for r in ("max", "pow2", "exact")] + \
+        [("paged", "max", bs) for bs in (1, 8, 16, 32, 64, 128)]
+    rows = []
+    t0 = time.perf_counter()
+    for alloc, rule, bs in runs:
+        r = pa.simulate_allocator(a, p, o, alloc, cap, block_size=bs, reserve=rule,
+                                  max_seq_len=s.max_seq_len)
+        row = {"allocator": alloc if alloc == "paged" else f"contiguous/{rule}",
+               "block_size": bs if alloc == "paged" else None,
+               "kv_utilisation": round(r["utilisation_of_held"], 4),
+               "utilisation_of_pool": round(r["utilisation_of_capacity"], 4),
+               "max_concurrency": r["max_concurrency"],
+               "mean_concurrency": round(r["mean_concurrency"], 1),
+               "failed_allocations": r["failed_allocations"],
+               "fragmentation_failures": r["fragmentation_failures"],
+               "preemptions": r["preemptions"], "steps": r["steps"]}
+        if alloc == "paged":
+            row["internal_fragmentation"] = round(r["internal_fragmentation"], 4)
+            row["mean_block_table_len"] = round(r["mean_table_len"], 2)
+            row["max_block_table_len"] = r["max_table_len"]
+        rows.append(row)
+    native_s = time.perf_counter() - t0
+    oracle_s = None
+    if not args.no_cpu_baseline:
+        from oracle.allocator_sim import simulate, CONTIGUOUS, PAGED, RESERVE_MAX
+        t0 = time.perf_counter()
+        simulate(a, p, o, PAGED, capacity=cap, block_size=16, max_seq_len=s.max_seq_len)
+        simulate(a, p, o, CONTIGUOUS, capacity=cap, reserve=RESERVE_MAX,
+                 max_seq_len=s.max_seq_len)
+        oracle_s = time.perf_counter() - t0
+    paged16 = next(r for r in rows if r["block_size"] == 16)
+    contig = rows[0]
+    return {
+        "metric": "KV memory utilisation, paged (block 16) vs contiguous (max reservation)",
+        "value": paged16["kv_utilisation"], "unit": "fraction", "op": "allocsim",
+        "higher_is_better": True, "data": "synthetic request stream (seeded)",
+        "config": {"workload": "serving_stream", "requests": s.num_requests,
+                   "arrivals_per_step": s.rate, "prompt": f"lognormal median {s.prompt_median:g} "
+                   f"sigma {s.prompt_sigma:g}", "output": f"lognormal median {s.output_median:g} "
+                   f"sigma {s.output_sigma:g}", "max_seq_len": s.max_seq_len,
+                   "capacity_tokens": cap},
+        "contiguous_max_utilisation": contig["kv_utilisation"],
+        "concurrency_gain": round(paged16["max_concurrency"] / contig["max_concurrency"], 2),
+        "sweep": rows,
+        "native_s_for_sweep": round(native_s, 3),
+        "oracle_s_for_two_runs": None if oracle_s is None else round(oracle_s, 3),
+        "gpu_launches": 0,
+    }
+
+
 # ----------------------------------------------------------------------------
 # CPU oracle (baseline leg and the reference arm)
 # ----------------------------------------------------------------------------
@@ -729,9 +790,11 @@ def main():
     ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_head"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--op", choices=["decode", "swap", "cow_layers"], default="decode",
+    ap.add_argument("--op", choices=["decode", "swap", "cow_layers", "allocsim"],
+                    default="decode",
                     help="decode: the decode step (default); swap / cow_layers: whole-block "
-                         "moves over a 32-layer model's pools")
+                         "moves over a 32-layer model's pools; allocsim: contiguous vs paged "
+                         "allocator simulation (host only)")
     ap.add_argument("--pairs", type=int, default=512, help="blocks per pool moved (--op swap, "
                                                            "cow_layers)")
     args = ap.parse_args()
@@ -741,6 +804,8 @@ def main():
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "op": args.op,
                               "unavailable": "no CPU arm for block moves"}), flush=True)
+        elif args.op == "allocsim":
+            print(json.dumps(run_allocsim(args)), flush=True)
         else:
             print(json.dumps(run_blocks(args)), flush=True)
         return

@@ -348,6 +348,72 @@ int pa_bm_seq_num_blocks(const pa_block_manager* bm, int seq_id);
 pa_status pa_bm_export(const pa_block_manager* bm, const int* seq_ids, int n, int max_blocks,
                        int32_t pad_id, int32_t* block_tables, int32_t* seq_lens);
 
+/* ------------------------------------------------------------------------ */
+/* Allocator simulator                                                       */
+/* ------------------------------------------------------------------------ */
+/*
+ * A contiguous and a paged KV allocator serving one request stream
+ * ("10 — Paged Attention" tutorial, §10 exercises B and C; the 20-38% vs 96%+
+ * memory-utilisation comparison of §7).  Host code.  Time advances in decode
+ * steps t = 0, 1, ...; each step:
+ *   1. requests with arrival_step <= t join the back of the waiting queue;
+ *   2. admission: the queue head is admitted while its allocation succeeds; the
+ *      first failure ends admission for the step (one failed allocation);
+ *      an admitted request holds len tokens (its prompt, or after a preemption
+ *      all it had: the KV is recomputed);
+ *   3. growth: each request admitted in an earlier step, in admission order,
+ *      appends one token; paged: with its blocks full it takes one more block,
+ *      or, with none free, is preempted (one failed allocation, one preemption):
+ *      its blocks are freed and it goes back to the front of the queue (those
+ *      preempted in one step in admission order);
+ *   4. measurement (when any request runs): tokens stored = sum of len, memory
+ *      held (contiguous: sum of reservations; paged: blocks x block_size),
+ *      running requests, blocks per request (paged);
+ *   5. requests with len == prompt + output finish and release their memory.
+ * Contiguous: one extent of `reserve` slots of a linear space of
+ * capacity_tokens, first fit at the lowest address, freed extents merged;
+ * reserve = max_seq_len (MAX), next power of two of prompt + output (POW2) or
+ * prompt + output (EXACT).  A failed admission while the free total covers the
+ * request is also a fragmentation failure.  Paged: capacity_tokens / block_size
+ * blocks, admission needs ceil(len / block_size) free blocks.
+ * Requests: arrival_step non-decreasing; 1 <= prompt, 1 <= output,
+ * prompt + output <= max_seq_len; each must fit an empty pool.  Stops after
+ * max_steps steps (result.completed < num_requests then).
+ */
+enum { PA_SIM_CONTIGUOUS = 0, PA_SIM_PAGED = 1 };
+enum { PA_SIM_RESERVE_MAX = 0, PA_SIM_RESERVE_POW2 = 1, PA_SIM_RESERVE_EXACT = 2 };
+
+typedef struct {
+  int allocator;              /* PA_SIM_CONTIGUOUS or PA_SIM_PAGED */
+  int reserve;                /* contiguous reservation rule, PA_SIM_RESERVE_* */
+  int block_size;             /* paged */
+  int max_seq_len;            /* longest request; the MAX reservation */
+  int64_t capacity_tokens;    /* KV slots of the pool */
+  int64_t max_steps;
+} pa_sim_config;
+
+typedef struct {
+  int64_t steps;                    /* steps simulated */
+  int64_t completed;                /* requests finished */
+  int64_t failed_allocations;       /* failed admissions + failed growths */
+  int64_t fragmentation_failures;   /* contiguous: failed although enough was free */
+  int64_t preemptions;              /* paged: growths that found no free block */
+  int64_t max_concurrency;          /* most requests running in one step */
+  int64_t sum_concurrency;          /* sums over the steps with a running request: */
+  int64_t busy_steps;               /*   that many steps */
+  int64_t sum_stored;               /*   tokens stored */
+  int64_t sum_held;                 /*   slots held by the allocator */
+  int64_t peak_stored, peak_held;
+  int64_t sum_table_len;            /* paged: blocks held, summed over requests and steps */
+  int64_t max_table_len;            /* paged: longest block table */
+} pa_sim_result;
+
+/* Arrays of num_requests int32 in host memory.  PA_ERR_INVALID_ARG on a bad
+ * configuration or request (nothing simulated). */
+pa_status pa_sim_run(const pa_sim_config* cfg, const int32_t* arrival_step,
+                     const int32_t* prompt_len, const int32_t* output_len, int num_requests,
+                     pa_sim_result* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -228,6 +228,52 @@ def pa_append_tokens(k_pool: torch.Tensor, v_pool: torch.Tensor, key: torch.Tens
     _check(st, "pa_append_tokens")
 
 
+class _SimConfig(ctypes.Structure):
+    _fields_ = [("allocator", ctypes.c_int), ("reserve", ctypes.c_int),
+                ("block_size", ctypes.c_int), ("max_seq_len", ctypes.c_int),
+                ("capacity_tokens", ctypes.c_int64), ("max_steps", ctypes.c_int64)]
+
+
+_SIM_FIELDS = ("steps", "completed", "failed_allocations", "fragmentation_failures",
+               "preemptions", "max_concurrency", "sum_concurrency", "busy_steps", "sum_stored",
+               "sum_held", "peak_stored", "peak_held", "sum_table_len", "max_table_len")
+
+
+class _SimResult(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int64) for f in _SIM_FIELDS]
+
+
+SIM_ALLOCATORS = {"contiguous": 0, "paged": 1}
+SIM_RESERVE = {"max": 0, "pow2": 1, "exact": 2}
+
+
+def simulate_allocator(arrival_step, prompt_len, output_len, allocator: str, capacity: int,
+                       block_size: int = 16, reserve: str = "max", max_seq_len: int = 2048,
+                       max_steps: int = 10_000_000) -> dict:
+    """Contiguous or paged KV allocator over a request stream (pa_sim_run);
+    returns the integer counters plus the derived ratios."""
+    import numpy as np
+    a = np.ascontiguousarray(arrival_step, dtype=np.int32)
+    p = np.ascontiguousarray(prompt_len, dtype=np.int32)
+    o = np.ascontiguousarray(output_len, dtype=np.int32)
+    if not len(a) == len(p) == len(o):
+        raise ValueError("one arrival, prompt and output length per request")
+    cfg = _SimConfig(SIM_ALLOCATORS[allocator], SIM_RESERVE[reserve], block_size, max_seq_len,
+                     capacity, max_steps)
+    res = _SimResult()
+    _check(lib().pa_sim_run(ctypes.byref(cfg), a.ctypes.data, p.ctypes.data, o.ctypes.data,
+                            len(a), ctypes.byref(res)), "pa_sim_run")
+    out = {f: int(getattr(res, f)) for f in _SIM_FIELDS}
+    busy = max(out["busy_steps"], 1)
+    out["utilisation_of_held"] = out["sum_stored"] / max(out["sum_held"], 1)
+    out["utilisation_of_capacity"] = out["sum_stored"] / (busy * max(capacity, 1))
+    out["mean_concurrency"] = out["sum_concurrency"] / busy
+    if allocator == "paged":
+        out["internal_fragmentation"] = 1.0 - out["utilisation_of_held"]
+        out["mean_table_len"] = out["sum_table_len"] / max(out["sum_concurrency"], 1)
+    return out
+
+
 class BlockManager:
     """Host block manager of libpagedattn (pa_bm_*): allocate / free / fork and
     sequences that append one token at a time with copy-on-write."""
@@ -330,5 +376,5 @@ __all__ = [
     "pa_decode_noalloc", "set_decode_path",
     "alloc_workspace", "pa_reshape_and_cache", "pa_append_tokens",
     "pa_copy_blocks_multi", "pa_swap_blocks", "pa_copy_blocks", "pa_decode_slots",
-    "BlockManager", "lib",
+    "BlockManager", "lib", "simulate_allocator",
 ]

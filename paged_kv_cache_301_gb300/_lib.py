@@ -44,6 +44,7 @@ SIGNATURES = {
     "pa_decode_slots": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p]),
     "pa_bm_create": (c_int, [c_int, c_int, c_void_p, ctypes.POINTER(c_void_p)]),
     "pa_bm_destroy": (None, [c_void_p]),
+    "pa_sim_run": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "pa_bm_num_free": (c_int, [c_void_p]),
     "pa_bm_num_evictable": (c_int, [c_void_p]),
     "pa_bm_seq_create_cached": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(c_int),

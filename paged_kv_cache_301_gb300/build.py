@@ -25,6 +25,7 @@ SOURCES = [
     "pa_cache.cu",
     "pa_decode_simt.cu",
     "pa_block_manager.cpp",
+    "pa_allocsim.cpp",
     "pa_decode_noalloc.cu",
     "pa_decode_tc.cu",
     "pa_decode_tcg.cu", "pa_blocks.cu",

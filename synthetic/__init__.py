@@ -207,3 +207,48 @@ def pool_fill_bits(w: Workload, num_blocks: int, sub: int = 0, chunk_blocks: int
         k[lo:hi] = normal_bits(g, (hi - lo,) + shape[1:], w.dtype)
         v[lo:hi] = normal_bits(g, (hi - lo,) + shape[1:], w.dtype)
     return k, v
+
+
+# ----------------------------------------------------------------------------
+# request streams for the allocator simulator
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class RequestStream:
+    """A serving request stream: Poisson arrivals (exponential gaps, counted in
+    decode steps) and lognormal prompt and output lengths (the tutorial's
+    simulator exercise, §10 B).  Lengths are clipped so that prompt + output
+    never exceeds max_seq_len."""
+
+    name: str
+    seed: int
+    num_requests: int
+    rate: float                  # mean arrivals per decode step
+    prompt_median: float
+    prompt_sigma: float
+    output_median: float
+    output_sigma: float
+    max_seq_len: int
+
+
+SERVING_STREAM = RequestStream(
+    name="serving", seed=11, num_requests=4000, rate=4.0, prompt_median=256.0,
+    prompt_sigma=1.0, output_median=128.0, output_sigma=1.0, max_seq_len=2048)
+
+SMALL_STREAM = RequestStream(
+    name="small", seed=12, num_requests=300, rate=2.0, prompt_median=40.0, prompt_sigma=1.0,
+    output_median=24.0, output_sigma=0.8, max_seq_len=256)
+
+
+def request_arrays(s: RequestStream) -> tuple:
+    """(arrival_step, prompt_len, output_len), int32 arrays of num_requests,
+    arrival steps non-decreasing; prompt >= 1, output >= 1, sum <= max_seq_len."""
+    g = np.random.default_rng([s.seed, 7])
+    gaps = g.exponential(1.0 / s.rate, size=s.num_requests)
+    arrival = np.floor(np.cumsum(gaps)).astype(np.int64)
+    p = np.rint(np.exp(math.log(s.prompt_median) + s.prompt_sigma * g.standard_normal(s.num_requests)))
+    o = np.rint(np.exp(math.log(s.output_median) + s.output_sigma * g.standard_normal(s.num_requests)))
+    p = np.clip(p, 1, s.max_seq_len - 1).astype(np.int64)
+    o = np.clip(o, 1, None).astype(np.int64)
+    o = np.minimum(o, s.max_seq_len - p)
+    return arrival.astype(np.int32), p.astype(np.int32), o.astype(np.int32)
