@@ -313,3 +313,30 @@ def swap_round_trip(batch: PagedBatch, swapped, cpu_num_blocks: int,
     after.block_tables = _tables(seqs, after.pad_block, batch.max_blocks)
     return SwapRoundTrip(batch, after, cpu_num_blocks, out_arr, in_arr,
                          np.asarray(reused, dtype=np.int32), cpu_k_out, cpu_v_out)
+
+
+@dataclasses.dataclass
+class PrefillBatch:
+    batch: PagedBatch            # pools, tables, lengths (KV of every token written)
+    q: np.ndarray                # [total_q, Hq, D] uint16 storage bits
+    q_start: np.ndarray          # [B + 1] int32
+
+
+def prefill_batch(w: syn.Workload, lens=None, q_counts=None, block_size: Optional[int] = None,
+                  fill_all: bool = False) -> PrefillBatch:
+    """A paged batch holding every token's KV plus queries for the last
+    q_counts[b] tokens of each sequence (all of them for a whole-prompt
+    prefill)."""
+    batch = fixed_batch(w, lens=lens, block_size=block_size, fill_all=fill_all)
+    n = syn.query_counts(w, batch.seq_lens) if q_counts is None else \
+        np.asarray(q_counts, dtype=np.int64)
+    q_start = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    q = syn.prefill_query_bits(w, int(q_start[-1]))
+    return PrefillBatch(batch, q, q_start)
+
+
+def prefill_f64(pb: PrefillBatch, rows=None) -> np.ndarray:
+    from .prefill import paged_prefill_attention
+    b = pb.batch
+    return paged_prefill_attention(pb.q, b.k_pool, b.v_pool, b.block_tables, b.seq_lens,
+                                   pb.q_start, b.scale, dtype=b.dtype, rows=rows)

@@ -61,6 +61,10 @@ class Workload:
     prefix_jitter: int = 0       # extra prompt tokens drawn from U{0..jitter}
     tail_lo: int = 0
     tail_hi: int = 0
+    # prefill workloads: query tokens per sequence, "" (decode: one), "full"
+    # (the whole prompt) or "chunk" (the last min(L, chunk) tokens)
+    prefill: str = ""
+    chunk: int = 0
 
     @property
     def group(self) -> int:
@@ -105,14 +109,28 @@ RAGGED = Workload(
 
 RAGGED_BLOCK_SIZES = (8, 16, 32, 64)
 
-WORKLOADS = {w.name: w for w in (TINY, LLAMA3_8B, SHARED_PREFIX, LONG_CONTEXT, RAGGED)}
+# Prefill: whole prompts of U[512, 4096] tokens; chunked prefill: the last 512
+# tokens of sequences of U[1024, 8192] tokens whose earlier tokens are cached.
+PREFILL = Workload(
+    name="prefill", num_seqs=8, num_q_heads=32, num_kv_heads=8, head_dim=128,
+    block_size=16, dtype=BFLOAT16, seed=5, length_kind="uniform", lo=512, hi=4096,
+    prefill="full")
+
+CHUNKED_PREFILL = Workload(
+    name="chunked_prefill", num_seqs=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+    block_size=16, dtype=BFLOAT16, seed=6, length_kind="uniform", lo=1024, hi=8192,
+    prefill="chunk", chunk=512)
+
+WORKLOADS = {w.name: w for w in (TINY, LLAMA3_8B, SHARED_PREFIX, LONG_CONTEXT, RAGGED,
+                                  PREFILL, CHUNKED_PREFILL)}
 
 
 # ----------------------------------------------------------------------------
 # random streams
 # ----------------------------------------------------------------------------
 
-_STREAMS = {"lens": 1, "values": 2, "free": 3, "query": 4, "new_kv": 5, "tails": 6}
+_STREAMS = {"lens": 1, "values": 2, "free": 3, "query": 4, "new_kv": 5, "tails": 6,
+            "prefill_query": 7}
 
 
 def rng(w: Workload, stream: str, sub: int = 0) -> np.random.Generator:
@@ -252,3 +270,19 @@ def request_arrays(s: RequestStream) -> tuple:
     o = np.clip(o, 1, None).astype(np.int64)
     o = np.minimum(o, s.max_seq_len - p)
     return arrival.astype(np.int32), p.astype(np.int32), o.astype(np.int32)
+
+
+def query_counts(w: Workload, lens) -> np.ndarray:
+    """Query tokens per sequence of a prefill workload."""
+    lens = np.asarray(lens, dtype=np.int64)
+    if w.prefill == "full":
+        return lens.copy()
+    if w.prefill == "chunk":
+        return np.minimum(lens, w.chunk)
+    return np.minimum(lens, 1)
+
+
+def prefill_query_bits(w: Workload, total_q: int, sub: int = 0) -> np.ndarray:
+    """Queries of a prefill batch, [total_q, Hq, D] storage bits."""
+    return normal_bits(rng(w, "prefill_query", sub), (total_q, w.num_q_heads, w.head_dim),
+                       w.dtype)
