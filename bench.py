@@ -557,6 +557,100 @@ def run_blocks(args):
     }
 
 
+def run_prefill(args):
+    """--op prefill: causal multi-query attention over the paged pool (pa_prefill)
+    on the whole-prompt or the chunked-prefill workload; FLOP/s of the causal
+    (query, key) pairs against the measured bf16 tensor peak."""
+    import torch
+    import paged_kv_cache_301_gb300 as pa
+    from paged_kv_cache_301_gb300 import build as _build
+    from oracle import scenarios
+    from oracle.prefill import causal_pairs
+
+    _build.build()
+    name = args.workload if args.workload in ("prefill", "chunked_prefill") else "prefill"
+    w = syn.WORKLOADS[name]
+    pb = scenarios.prefill_batch(w, fill_all=True)
+    b = pb.batch
+    torch.cuda.set_device(0)
+    dt = {syn.FLOAT16: torch.float16, syn.BFLOAT16: torch.bfloat16}[w.dtype]
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(dt)
+
+    kp, vp, q = dev(b.k_pool), dev(b.v_pool), dev(pb.q)
+    tables = torch.from_numpy(b.block_tables).cuda()
+    lens = torch.from_numpy(b.seq_lens).cuda()
+    qst = torch.from_numpy(pb.q_start).cuda()
+    out = torch.empty_like(q)
+    max_q = int(np.diff(pb.q_start).max())
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pa.pa_prefill(out, q, kp, vp, tables, lens, qst, w.scale, max_q_len=max_q)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_uuid(torch, torch.device("cuda", 0)))
+    clocks.start()
+    time.sleep(0.25)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    pairs = causal_pairs(b.seq_lens, pb.q_start)
+    flops = 4.0 * w.head_dim * w.num_q_heads * pairs          # q.k and p.v per pair and head
+    tflops = flops / (ms * 1e-3) / 1e12
+    total_q = int(pb.q_start[-1])
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("bf16_tflops") or 1900.0
+    peak_kind = "measured (cuBLAS bf16, burst)" if "bf16_tflops" in peaks else "fallback"
+    cpu = None
+    if not args.no_cpu_baseline:
+        g = np.random.default_rng(3)
+        rows = sorted(set(int(x) for x in g.integers(0, total_q, size=16)))
+        t0 = time.perf_counter()
+        scenarios.prefill_f64(pb, rows=rows)
+        el = time.perf_counter() - t0
+        # flops of the sampled rows: each row sees position + 1 keys, all heads
+        pos = []
+        for r in rows:
+            s_ = int(np.searchsorted(pb.q_start, r, side="right")) - 1
+            n_ = int(pb.q_start[s_ + 1] - pb.q_start[s_])
+            pos.append(int(b.seq_lens[s_]) - n_ + (r - int(pb.q_start[s_])))
+        f_rows = 4.0 * w.head_dim * w.num_q_heads * sum(p_ + 1 for p_ in pos)
+        cpu = {"value": round(f_rows / el / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+               "kind": "oracle", "sample": f"{len(rows)} query rows (all heads) of the {name} "
+                                           f"workload, fp64 oracle, {el:.1f} s"}
+    return {
+        "metric": "paged prefill attention TFLOP/s (causal pairs x 4 x head_dim x heads)",
+        "value": round(tflops, 1), "unit": "TFLOP/s", "op": "prefill", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "dtype": syn.DTYPE_NAMES[w.dtype],
+        "data": "synthetic (seeded N(0,1) q/K/V; block ids a seeded permutation)",
+        "config": {"workload": name, "num_seqs": len(b.seq_lens), "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "total_tokens": int(b.seq_lens.sum()),
+                   "query_tokens": total_q, "causal_pairs_per_head": pairs},
+        "tokens_per_s": round(total_q / (ms * 1e-3), 1),
+        "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor",
+                     "achieved": round(tflops, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                     "algorithmic_flops": flops, "avg_launch_ms": round(ms, 5)},
+        "clocks": clk, "cpu_baseline": cpu, "gpu_launches": args.steps,
+    }
+
+
 def run_allocsim(args):
     """--op allocsim: contiguous vs paged KV allocation on a saturated serving
     stream (Poisson arrivals, lognormal lengths), block-size sweep; host code
@@ -784,28 +878,34 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="llama3_8b",
-                    choices=["llama3_8b", "long_context", "shared_prefix", "ragged", "tiny"])
+                    choices=["llama3_8b", "long_context", "shared_prefix", "ragged", "tiny",
+                             "prefill", "chunked_prefill"])
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_head"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--op", choices=["decode", "swap", "cow_layers", "allocsim"],
+    ap.add_argument("--op", choices=["decode", "swap", "cow_layers", "allocsim", "prefill"],
                     default="decode",
                     help="decode: the decode step (default); swap / cow_layers: whole-block "
                          "moves over a 32-layer model's pools; allocsim: contiguous vs paged "
-                         "allocator simulation (host only)")
+                         "allocator simulation (host only); prefill: paged causal "
+                         "multi-query attention (--workload prefill | chunked_prefill)")
     ap.add_argument("--pairs", type=int, default=512, help="blocks per pool moved (--op swap, "
                                                            "cow_layers)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.op == "decode" and args.workload in ("prefill", "chunked_prefill"):
+        ap.error("the prefill workloads run with --op prefill")
     if args.op != "decode":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "op": args.op,
                               "unavailable": "no CPU arm for block moves"}), flush=True)
         elif args.op == "allocsim":
             print(json.dumps(run_allocsim(args)), flush=True)
+        elif args.op == "prefill":
+            print(json.dumps(run_prefill(args)), flush=True)
         else:
             print(json.dumps(run_blocks(args)), flush=True)
         return

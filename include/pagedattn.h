@@ -244,6 +244,38 @@ pa_status pa_append_tokens(void* k_pool, void* v_pool, const void* key, const vo
                            int num_blocks, int dtype, int32_t* status_dev, cudaStream_t stream);
 
 /*
+ * Paged multi-query attention with a causal mask: prefill, chunked prefill and
+ * verification of several drafted tokens (subroutine-cs article, introduction:
+ * the prefill phase computes all prompt tokens at once; "10 — Paged Attention"
+ * §5 "The kernel side" for the gather through the block table).
+ *   q, out      [total_q, num_q_heads, head_dim]; rows q_start[b] .. q_start[b+1]-1
+ *               are sequence b's n_b = q_start[b+1] - q_start[b] query tokens,
+ *               which are its LAST n_b tokens: row q_start[b] + i is position
+ *               seq_lens[b] - n_b + i.  Their K/V must already be in the pool
+ *               (pa_reshape_and_cache).
+ *   q_start     [num_seqs + 1] int32, non-decreasing, q_start[0] = 0,
+ *               q_start[num_seqs] = total_q (device memory).
+ *   max_q_len   host upper bound of every n_b (sizes the grid, no device sync).
+ * For query head hq of that row, with KV head h = hq / (num_q_heads /
+ * num_kv_heads):  out = softmax_t(scale * q . K[slot_t, h]) . V[slot_t, h] over
+ * t = 0 .. position, slot_t as in pa_decode.  fp32 accumulation, output rounded
+ * to the storage type.  Supported: head_dim 128, num_q_heads / num_kv_heads in
+ * {1, 2, 4, 8, 16}, block_size in {8, 16, 32, 64}; other shapes return
+ * PA_ERR_UNSUPPORTED.  A sequence with n_b > seq_lens[b], n_b > max_q_len,
+ * seq_lens[b] > max_blocks * block_size, or rows outside [0, total_q) is skipped
+ * (rows untouched; reported in checked mode); out-of-range block ids read zeros
+ * (reported in checked mode).
+ * No workspace.  Kernel: tcgen05 tensor cores, TMA, one CTA per (sequence, KV
+ * head, tile of 128 / G query tokens x G heads).
+ */
+pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* block_tables, const int32_t* seq_lens,
+                     const int32_t* q_start, int num_seqs, int total_q, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                     int num_blocks, int max_q_len, float scale, int dtype,
+                     int32_t* status_dev, cudaStream_t stream);
+
+/*
  * Copy-on-write across a whole model in one launch ("10 — Paged Attention"
  * tutorial §5 "Copy-on-write sharing"; a model keeps one K and one V pool per
  * layer, subroutine-cs article §1 bytes-per-token formula).  For every pair

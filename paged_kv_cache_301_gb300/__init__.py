@@ -213,6 +213,25 @@ def pa_decode_slots(slot_mapping: torch.Tensor, block_tables: torch.Tensor,
     return slot_mapping
 
 
+def pa_prefill(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+               block_tables: torch.Tensor, seq_lens: torch.Tensor, q_start: torch.Tensor,
+               scale: float, max_q_len: Optional[int] = None,
+               status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal attention of each sequence's last n_b tokens (q rows q_start[b] ..
+    q_start[b+1]-1) over its paged K/V.  max_q_len: host bound of n_b (computed
+    from q_start, with a device sync, when omitted)."""
+    total_q, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_pool.shape
+    B, MB = block_tables.shape
+    if max_q_len is None:
+        max_q_len = int((q_start[1:] - q_start[:-1]).max().item()) if B else 0
+    st = lib().pa_prefill(_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                          _ptr(seq_lens), _ptr(q_start), B, total_q, Hq, Hkv, D, bs, MB, NB,
+                          max_q_len, float(scale), _dtype(q), _ptr(status), _stream(stream))
+    _check(st, "pa_prefill")
+    return out
+
+
 def pa_append_tokens(k_pool: torch.Tensor, v_pool: torch.Tensor, key: torch.Tensor,
                      value: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
                      slot_mapping: Optional[torch.Tensor] = None,
@@ -374,7 +393,7 @@ class BlockManager:
 __all__ = [
     "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_workspace_bytes",
     "pa_decode_noalloc", "set_decode_path",
-    "alloc_workspace", "pa_reshape_and_cache", "pa_append_tokens",
+    "alloc_workspace", "pa_reshape_and_cache", "pa_append_tokens", "pa_prefill",
     "pa_copy_blocks_multi", "pa_swap_blocks", "pa_copy_blocks", "pa_decode_slots",
     "BlockManager", "lib", "simulate_allocator",
 ]

@@ -34,6 +34,9 @@ SIGNATURES = {
     "pa_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_void_p, c_void_p]),
     "pa_set_decode_path": (c_int, [c_int]),
+    "pa_prefill": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                           c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                           ctypes.c_float, c_int, c_void_p, c_void_p]),
     "pa_copy_blocks_multi": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int64, c_int, c_void_p,
                                      c_void_p]),
     "pa_swap_blocks": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int64, c_int, c_int,

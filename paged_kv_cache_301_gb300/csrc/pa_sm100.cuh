@@ -109,6 +109,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Data other CTAs will read again soon: keep it in L2 ahead of streamed data.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // -------------------------------------------------------------- tcgen05 --
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -1,0 +1,143 @@
+"""GPU parity of pa_prefill (causal multi-query attention over the paged pool)
+against the fp64 oracle: every row on small batches that span several query and
+key tiles with ragged tails, sampled rows at the benchmark sizes, and the
+properties that hold at any size (causality, determinism, one query = decode)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic as syn
+from oracle import scenarios
+from tests.gpu_helpers import DeviceBatch, assert_close, i32, lib, to_dev, widen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    return lib()
+
+
+def _run(pa, pb, dev=None, status=None, max_q_len=None):
+    b = pb.batch
+    dev = dev or DeviceBatch(b)
+    q = to_dev(pb.q, b.dtype)
+    out = torch.full_like(q, float("nan"))
+    n = np.diff(pb.q_start)
+    pa.pa_prefill(out, q, dev.k_pool, dev.v_pool, dev.tables, dev.lens, i32(pb.q_start),
+                  b.scale, max_q_len=int(n.max()) if max_q_len is None else max_q_len,
+                  status=status)
+    return out, dev
+
+
+def _small(G, bs, dtype, lens, hkv=2):
+    return dataclasses.replace(syn.PREFILL, name=f"pf_g{G}_bs{bs}", num_seqs=len(lens),
+                               length_kind="fixed", lens=tuple(lens), num_kv_heads=hkv,
+                               num_q_heads=hkv * G, block_size=bs, dtype=dtype)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+def test_whole_prompts_every_row(pa, G, bs):
+    """Lengths that end mid-block, mid-tile and exactly on tile edges."""
+    w = _small(G, bs, syn.BFLOAT16, [1, 127, 128, 300, 37])
+    pb = scenarios.prefill_batch(w)
+    out, dev = _run(pa, pb)
+    torch.cuda.synchronize()
+    assert_close(widen(out), scenarios.prefill_f64(pb), f"G={G} bs={bs}")
+    assert dev.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", [syn.FLOAT16, syn.BFLOAT16])
+@pytest.mark.parametrize("q_counts", [(5, 1, 200, 0, 64), (1, 1, 1, 1, 1), (17, 33, 129, 3, 70)])
+def test_chunks_over_cached_prefix_every_row(pa, dtype, q_counts):
+    """The last n tokens of each sequence attend to the whole cached prefix plus
+    themselves; n = 0 leaves a sequence out, n = 1 is a decode step."""
+    w = _small(4, 16, dtype, [700, 33, 1000, 90, 70], hkv=4)
+    pb = scenarios.prefill_batch(w, q_counts=q_counts)
+    out, _ = _run(pa, pb)
+    torch.cuda.synchronize()
+    assert_close(widen(out), scenarios.prefill_f64(pb), f"chunks {q_counts}")
+
+
+def test_one_query_matches_decode(pa):
+    w = _small(4, 16, syn.BFLOAT16, [700, 33, 1000, 90, 1], hkv=8)
+    pb = scenarios.prefill_batch(w, q_counts=(1, 1, 1, 1, 1))
+    out, dev = _run(pa, pb)
+    dec = torch.empty_like(out)
+    pa.pa_decode(dec, to_dev(pb.q, w.dtype), dev.k_pool, dev.v_pool, dev.tables, dev.lens,
+                 w.scale, max_seq_len=1000)
+    torch.cuda.synchronize()
+    ref = scenarios.prefill_f64(pb)
+    assert_close(widen(out), ref, "prefill n=1")
+    assert_close(widen(dec), ref, "decode")
+
+
+def test_causal_mask_ignores_later_tokens(pa):
+    """Overwriting the K/V of each sequence's last token with a large value
+    changes only the last row of that sequence; every earlier row, for which the
+    token lies past its position, stays bit-identical (masked keys weigh exactly
+    zero)."""
+    w = _small(4, 16, syn.BFLOAT16, [300, 129, 64], hkv=2)
+    pb = scenarios.prefill_batch(w)
+    out1, dev = _run(pa, pb)
+    b = pb.batch
+    for s, L in enumerate(b.seq_lens):
+        slot = int(b.block_tables[s][(L - 1) // b.block_size]) * b.block_size + (L - 1) % b.block_size
+        dev.k_pool.view(-1, w.num_kv_heads, w.head_dim)[slot] = 3.0e4
+        dev.v_pool.view(-1, w.num_kv_heads, w.head_dim)[slot] = 3.0e4
+    out2, _ = _run(pa, pb, dev=dev)
+    torch.cuda.synchronize()
+    last = sorted(int(x) - 1 for x in pb.q_start[1:])
+    keep = [r for r in range(out1.shape[0]) if r not in set(last)]
+    assert torch.equal(out1[keep].view(torch.int16), out2[keep].view(torch.int16))
+    assert not torch.equal(out1[last].view(torch.int16), out2[last].view(torch.int16))
+
+
+def test_deterministic_and_bad_input_reported(pa):
+    w = _small(8, 32, syn.BFLOAT16, [500, 260], hkv=4)
+    pb = scenarios.prefill_batch(w)
+    a, dev = _run(pa, pb)
+    c, _ = _run(pa, pb, dev=dev)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+    # more queries than tokens in sequence 1: reported, its rows untouched (NaN)
+    bad = dataclasses.replace(pb, q_start=np.array([0, 500, 761], dtype=np.int32),
+                              q=np.concatenate([pb.q, pb.q[:1]]))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _ = _run(pa, bad, dev=dev, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
+    assert torch.isnan(out[500:].float()).all()
+    assert torch.equal(out[:500].view(torch.int16), a[:500].view(torch.int16))
+
+
+def test_unsupported_shapes_refused(pa):
+    w = _small(4, 16, syn.BFLOAT16, [10], hkv=2)
+    pb = scenarios.prefill_batch(w)
+    dev = DeviceBatch(pb.batch)
+    q = to_dev(pb.q, w.dtype)
+    out = torch.empty_like(q)
+    with pytest.raises(pa.PagedAttnError) as ei:
+        pa.pa_prefill(out[:, :, :64].contiguous(), q[:, :, :64].contiguous(), dev.k_pool[..., :64].contiguous(),
+                      dev.v_pool[..., :64].contiguous(), dev.tables, dev.lens, i32(pb.q_start),
+                      w.scale, max_q_len=10)
+    assert ei.value.status == 2
+
+
+@pytest.mark.parametrize("w", [syn.PREFILL, syn.CHUNKED_PREFILL], ids=lambda w: w.name)
+def test_benchmark_workloads_sampled_rows(pa, w):
+    """Full size, in the launch configuration the benchmark times; the oracle
+    checks 48 rows spread over every sequence, first and last rows included."""
+    pb = scenarios.prefill_batch(w)
+    out, dev = _run(pa, pb)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(9)
+    rows = set(int(x) for x in pb.q_start[:-1]) | set(int(x) - 1 for x in pb.q_start[1:])
+    rows |= set(int(x) for x in g.integers(0, int(pb.q_start[-1]), size=48 - len(rows)))
+    rows = sorted(rows)
+    ref = scenarios.prefill_f64(pb, rows=rows)
+    assert_close(widen(out)[rows], ref[rows], w.name)
+    assert dev.guards_intact()
