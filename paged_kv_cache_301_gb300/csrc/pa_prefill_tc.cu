@@ -18,9 +18,10 @@
 //   O_t   = P . V_tile   [128 x D]             (TMEM, 2 buffers)
 //   acc  <- acc * exp2(m_old - m_new) + O_t    (registers: thread r owns row r)
 //
-// Roles (192 threads): warp 0 issues TMA (Q once, then K(t) before V(t-1) into a
-// ring of 32 KB stages), warp 1 issues tcgen05.mma, warps 2-5 run the softmax
-// and own the output rows.  Every wait is bounded.
+// Roles (320 threads): warp 0 issues TMA (Q once, then K(t) before V(t-1) into a
+// ring of 32 KB stages), warp 1 issues tcgen05.mma, warps 2-9 run the softmax
+// and own the output rows, two warps per row (64 keys and 64 output columns
+// each).  Every wait is bounded.
 #include <math_constants.h>
 
 #include <mutex>
@@ -41,10 +42,10 @@ constexpr int kTile = 2 * kSlab;            // 128 rows x 256 bytes (D = 128, 16
 constexpr int kQOff = 0;
 constexpr int kPOff = kQOff + kTile;        // P hi, then P lo
 constexpr int kRingOff = kPOff + 2 * kTile;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;                // producer, MMA, 8 softmax warps
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kSmemBudget = 232448 - 1024;  // per-block limit minus alignment slack
-constexpr int kTailBytes = 1024;
+constexpr int kTailBytes = 4096;
 constexpr int kStages = (kSmemBudget - kRingOff - kTailBytes) / kTile > 4
                             ? 4 : (kSmemBudget - kRingOff - kTailBytes) / kTile;
 constexpr uint32_t kTmemCols = 512;          // S[2] at 0 / 128, O[2] at 256 / 384
@@ -56,6 +57,9 @@ struct Tail {
   uint64_t p_full, p_empty;
   uint64_t o_full[2], o_empty[2];
   uint64_t drain;
+  uint64_t red_bar[2][4], sum_bar[4];          // the two warps of a lane quarter
+  float red_max[2][2][128];                    // [tile parity][half][row]
+  float red_sum[2][128];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -120,11 +124,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     mbar_init(&tl->q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tl->s_full[i], 1);
-      mbar_init(&tl->s_empty[i], 4);
+      mbar_init(&tl->s_empty[i], 8);
       mbar_init(&tl->o_full[i], 1);
-      mbar_init(&tl->o_empty[i], 4);
+      mbar_init(&tl->o_empty[i], 8);
+      for (int w = 0; w < 4; ++w) mbar_init(&tl->red_bar[i][w], 2);
     }
-    mbar_init(&tl->p_full, 4);
+    for (int w = 0; w < 4; ++w) mbar_init(&tl->sum_bar[w], 2);
+    mbar_init(&tl->p_full, 8);
     mbar_init(&tl->p_empty, 1);
     mbar_init(&tl->drain, 1);
     tl->abort_flag = 0;
@@ -268,85 +274,100 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
   else {
     // ------------------------------------------------ softmax and output rows --
+    // Two warps per TMEM lane quarter: `half` 0 takes keys 0-63 of each S tile and
+    // columns 0-63 of O, half 1 the other 64; they exchange row maxima per tile.
     const int wq = warp & 3;                     // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;
     const int r = wq * 32 + lane;                // tile row = query token r / G, head r % G
+    const int cb = half * 64;                    // this thread's first key / O column
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const int i = q0 + r / G;                    // query token within the sequence's queries
     const bool row_valid = i < n;
     const int pos = row_valid ? L - n + i : -1;  // keys 0 .. pos are visible
     float m_run = -CUDART_INF_F, l_run = 0.f, alpha_prev = 1.f;
-    float acc[kD];
+    float acc[64];
 #pragma unroll
-    for (int d = 0; d < kD; ++d) acc[d] = 0.f;
+    for (int d = 0; d < 64; ++d) acc[d] = 0.f;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, int parity) -> bool {
       const bool w = mbar_wait(bar, parity, abort_flag, kWaitNs);
       return __all_sync(0xFFFFFFFFu, w);
     };
-    // acc <- acc * alpha + O_u
+    // acc <- acc * alpha + O_u (this thread's 64 columns)
     auto accumulate = [&](int u, float alpha) -> bool {
       if (!wait_all(&tl->o_full[u & 1], (u >> 1) & 1)) return false;
       tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 16) {
-        float o[16];
-        tmem_ld16(tmem + lane_base + 256 + (u & 1) * kD + c0, o);
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        float o[32];
+        tmem_ld32(tmem + lane_base + 256 + (u & 1) * kD + cb + c0, o);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[c0 + e] = fmaf(acc[c0 + e], alpha, o[e]);
+        for (int e = 0; e < 32; ++e) acc[c0 + e] = fmaf(acc[c0 + e], alpha, o[e]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tl->o_empty[u & 1]);
       return true;
     };
-    uint8_t* prow = smem + kPOff + r * 128;      // row r of slab 0; slab 1 at +kSlab; lo at +kTile
+    uint8_t* prow = smem + kPOff + half * kSlab + r * 128;   // P hi row; lo at +kTile
+    const float sl2 = p.scale_log2;
     for (int t = 0; t <= last && ok; ++t) {
       const int sb = t & 1;
       if (!wait_all(&tl->s_full[sb], (t >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      const int k0 = t * kKeys;
-      const bool partial = k0 + kKeys - 1 > pos;   // some key of the tile is past this row
-      const uint32_t sadr = tmem + lane_base + sb * kKeys;
-      // pass 1: the tile's row maximum over visible keys
+      const int kc = t * kKeys + cb;             // key of this thread's first column
+      const bool partial = kc + 63 > pos;        // some of its keys lie past the row
+      const uint32_t sadr = tmem + lane_base + sb * kKeys + cb;
+      // pass 1: maximum of the visible raw scores (scale > 0 commutes with max)
       float mt = -CUDART_INF_F;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kKeys; c0 += 16) {
-        float s[16];
-        tmem_ld16(sadr + c0, s);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const bool keep = !partial || k0 + c0 + e <= pos;
-          mt = fmaxf(mt, keep ? s[e] * p.scale_log2 : -CUDART_INF_F);
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        float sv[32];
+        tmem_ld32(sadr + c0, sv);
+        if (!partial) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, sv[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, kc + c0 + e <= pos ? sv[e] : -CUDART_INF_F);
         }
       }
-      const float m_new = fmaxf(m_run, mt);
-      const float alpha = m_new == -CUDART_INF_F ? 1.f : exp2f(m_run - m_new);
-      // pass 2: p = exp2(s - m_new) into P (hi + lo), once the previous P.V is done
+      {   // row maximum over both halves
+        const int rb = t & 1;
+        tl->red_max[rb][half][r] = mt;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->red_bar[rb][wq]);
+        if (!wait_all(&tl->red_bar[rb][wq], (t >> 1) & 1)) { ok = false; break; }
+        mt = fmaxf(mt, tl->red_max[rb][half ^ 1][r]);
+      }
+      const float m_new = fmaxf(m_run, mt * sl2);
+      const float alpha = m_new == -CUDART_INF_F ? 1.f : ex2_approx(m_run - m_new);
+      const float neg_m = m_new == -CUDART_INF_F ? 0.f : -m_new;
+      // pass 2: p = 2^(s * scale * log2 e - m_new) into P (hi + lo), once the previous P.V is done
       if (!wait_all(&tl->p_empty, (t & 1) ^ 1)) { ok = false; break; }
       float ls = 0.f;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kKeys; c0 += 16) {
-        float s[16];
-        tmem_ld16(sadr + c0, s);
-        // keys c0 .. c0+15 = two 16-byte chunks of row r (128-byte swizzle), 8 keys each
-        const int slab = c0 >> 6;
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        float sv[32];
+        tmem_ld32(sadr + c0, sv);
+#pragma unroll
+        for (int c8 = 0; c8 < 32; c8 += 8) {     // 8 keys = one 16-byte chunk of the row
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
-            const int kk = c0 + 8 * hc + e;
-            const bool k_a = !partial || k0 + kk <= pos;
-            const bool k_b = !partial || k0 + kk + 1 <= pos;
-            const float pa_ = k_a ? exp2f(s[8 * hc + e] * p.scale_log2 - m_new) : 0.f;
-            const float pb_ = k_b ? exp2f(s[8 * hc + e + 1] * p.scale_log2 - m_new) : 0.f;
+            float pa_ = ex2_approx(fmaf(sv[c8 + e], sl2, neg_m));
+            float pb_ = ex2_approx(fmaf(sv[c8 + e + 1], sl2, neg_m));
+            if (partial) {
+              pa_ = kc + c0 + c8 + e <= pos ? pa_ : 0.f;
+              pb_ = kc + c0 + c8 + e + 1 <= pos ? pb_ : 0.f;
+            }
             ls += pa_ + pb_;
             const uint32_t h2 = narrow2<DT>(pa_, pb_);
             const float2 hf = widen2<DT>(h2);
             hi[e >> 1] = h2;
             lo[e >> 1] = narrow2<DT>(pa_ - hf.x, pb_ - hf.y);
           }
-          const int off = slab * kSlab + (((((c0 & 63) >> 3) + hc) ^ (r & 7)) << 4);
+          const int off = ((((c0 + c8) >> 3) ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(prow + kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
@@ -358,19 +379,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       m_run = m_new;
       // keys at or past L: their V rows hold whatever the slot or an earlier tile
       // left (0 * NaN must not reach O), so zero them before P.V reads the tile
+      const int k0 = t * kKeys;
       if (k0 + kKeys > L) {
         const int u = pos_v(t, last);
         const int vs = u % kStages, vph = (u / kStages) & 1;
         if (!wait_all(&tl->full[vs], vph)) { ok = false; break; }
         if (k0 + r >= L) {
-          uint4* v0 = reinterpret_cast<uint4*>(smem + kRingOff + vs * kTile + r * 128);
-          uint4* v1 = reinterpret_cast<uint4*>(smem + kRingOff + vs * kTile + kSlab + r * 128);
-          const uint4 z = make_uint4(0, 0, 0, 0);
+          uint4* v0 = reinterpret_cast<uint4*>(smem + kRingOff + vs * kTile + half * kSlab + r * 128);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            v0[e] = z;
-            v1[e] = z;
-          }
+          for (int e = 0; e < 8; ++e) v0[e] = make_uint4(0, 0, 0, 0);
         }
       }
       fence_async_smem();
@@ -380,14 +397,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       alpha_prev = alpha;
     }
     if (ok) ok = accumulate(last, alpha_prev);
+    if (ok) {   // row sum over both halves
+      tl->red_sum[half][r] = l_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tl->sum_bar[wq]);
+      ok = wait_all(&tl->sum_bar[wq], 0);
+    }
     if (!ok) {
       if (lane == 0) set_abort();
     } else if (row_valid) {
-      const float inv = 1.f / l_run;
+      const float inv = 1.f / (l_run + tl->red_sum[half ^ 1][r]);
       uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                          ((int64_t)(qs + i) * p.Hq + h * G + r % G) * kD);
+                                          ((int64_t)(qs + i) * p.Hq + h * G + r % G) * kD + cb);
 #pragma unroll
-      for (int c = 0; c < kD / 8; ++c)
+      for (int c = 0; c < 8; ++c)
         o[c] = make_uint4(narrow2<DT>(acc[8 * c] * inv, acc[8 * c + 1] * inv),
                           narrow2<DT>(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv),
                           narrow2<DT>(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv),
