@@ -14,8 +14,10 @@
 //
 //   S = Q_tile[128 x D] . K_tile^T            (TMEM, 128 fp32 columns, 2 buffers)
 //   row r: mask keys past its position, running max m, p = exp2(s - m)
-//   P     [128 x 128 keys] into shared memory as two storage-type terms hi + lo
-//   O_t   = P . V_tile   [128 x D]             (TMEM, 2 buffers)
+//   P     [128 x 128 keys] as two storage-type terms hi + lo, written to tensor
+//         memory over the S columns it replaces
+//   O_t   = P . V_tile   [128 x D]             (P from TMEM, V from shared memory;
+//                                              TMEM, 2 buffers)
 //   acc  <- acc * exp2(m_old - m_new) + O_t    (registers: thread r owns row r)
 //
 // Roles (320 threads): warp 0 issues TMA (Q once, then K(t) before V(t-1) into a
@@ -40,21 +42,22 @@ constexpr int kKeys = 128;                  // keys per KV tile (N of S, K of P.
 constexpr int kSlab = 128 * 128;            // 128 rows x 128 bytes
 constexpr int kTile = 2 * kSlab;            // 128 rows x 256 bytes (D = 128, 16-bit)
 constexpr int kQOff = 0;
-constexpr int kPOff = kQOff + kTile;        // P hi, then P lo
-constexpr int kRingOff = kPOff + 2 * kTile;
+constexpr int kRingOff = kQOff + kTile;
 constexpr int kThreads = 320;                // producer, MMA, 8 softmax warps
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kSmemBudget = 232448 - 1024;  // per-block limit minus alignment slack
 constexpr int kTailBytes = 4096;
-constexpr int kStages = (kSmemBudget - kRingOff - kTailBytes) / kTile > 4
-                            ? 4 : (kSmemBudget - kRingOff - kTailBytes) / kTile;
-constexpr uint32_t kTmemCols = 512;          // S[2] at 0 / 128, O[2] at 256 / 384
+constexpr int kStages = (kSmemBudget - kRingOff - kTailBytes) / kTile > 6
+                            ? 6 : (kSmemBudget - kRingOff - kTailBytes) / kTile;
+// TMEM: S/P[2] at columns 0 / 128 (P overwrites the S it was computed from),
+// O[2] at 256 / 384
+constexpr uint32_t kTmemCols = 512;
 
 struct Tail {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full;
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, p_empty;
+  uint64_t p_full;
   uint64_t o_full[2], o_empty[2];
   uint64_t drain;
   uint64_t red_bar[2][4], sum_bar[4];          // the two warps of a lane quarter
@@ -124,14 +127,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     mbar_init(&tl->q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tl->s_full[i], 1);
-      mbar_init(&tl->s_empty[i], 8);
+      mbar_init(&tl->s_empty[i], 1);
       mbar_init(&tl->o_full[i], 1);
       mbar_init(&tl->o_empty[i], 8);
       for (int w = 0; w < 4; ++w) mbar_init(&tl->red_bar[i][w], 2);
     }
     for (int w = 0; w < 4; ++w) mbar_init(&tl->sum_bar[w], 2);
     mbar_init(&tl->p_full, 8);
-    mbar_init(&tl->p_empty, 1);
     mbar_init(&tl->drain, 1);
     tl->abort_flag = 0;
     fence_mbar_init();
@@ -215,12 +217,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     // -------------------------------------------------------------- MMA issue --
     constexpr uint32_t ab = DT == PA_BFLOAT16 ? 1u : 0u;
     constexpr uint32_t idesc_s = idesc_f16(ab, 0, 0, kRows, kKeys);   // Q, K both K-major
-    constexpr uint32_t idesc_o = idesc_f16(ab, 0, 1, kRows, kD);      // P K-major, V MN-major
+    constexpr uint32_t idesc_o = idesc_f16(ab, 0, 1, kRows, kD);      // P (TMEM), V MN-major
     const uint32_t ring = smem_addr(smem + kRingOff);
     const uint32_t qaddr = smem_addr(smem + kQOff);
-    const uint32_t paddr = smem_addr(smem + kPOff);
     bool ok = true, committed = false;
-    // O_u = (P_hi + P_lo) . V_u into O buffer u & 1
+    // O_u = (P_hi + P_lo) . V_u into O buffer u & 1.  P sits in S buffer u & 1:
+    // 16-key group k occupies columns 16k .. 16k+7 (hi) and 16k+8 .. 16k+15 (lo).
     auto issue_pv = [&](int u) -> bool {
       const int vs = pos_v(u, last) % kStages, vph = (pos_v(u, last) / kStages) & 1;
       if (!mbar_wait(&tl->full[vs], vph, abort_flag, kWaitNs)) return false;
@@ -228,19 +230,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (!mbar_wait(&tl->o_empty[u & 1], ((u >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
       tc_fence_after();
       const uint32_t vaddr = ring + vs * kTile;
+      const uint32_t pcol = tmem + (u & 1) * kKeys;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int kk = 0; kk < kKeys / 16; ++kk) {
+        const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, kSlab, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(
-              paddr + half * kTile + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, kSlab, 1024);
-          mma_f16(tmem + 256 + (u & 1) * kD, a, bd, idesc_o, (half | kk) != 0);
-        }
+        for (int term = 0; term < 2; ++term)
+          mma_f16_ts(tmem + 256 + (u & 1) * kD, pcol + kk * 16 + term * 8, bd, idesc_o,
+                     (kk | term) != 0);
       }
       mma_commit(&tl->empty[vs]);
       mma_commit(&tl->o_full[u & 1]);
-      mma_commit(&tl->p_empty);
+      mma_commit(&tl->s_empty[u & 1]);      // S/P buffer free for S(u + 2)
       return true;
     };
     if (lane == 0) {
@@ -309,7 +310,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (lane == 0) mbar_arrive(&tl->o_empty[u & 1]);
       return true;
     };
-    uint8_t* prow = smem + kPOff + half * kSlab + r * 128;   // P hi row; lo at +kTile
     const float sl2 = p.scale_log2;
     for (int t = 0; t <= last && ok; ++t) {
       const int sb = t & 1;
@@ -343,38 +343,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       const float m_new = fmaxf(m_run, mt * sl2);
       const float alpha = m_new == -CUDART_INF_F ? 1.f : ex2_approx(m_run - m_new);
       const float neg_m = m_new == -CUDART_INF_F ? 0.f : -m_new;
-      // pass 2: p = 2^(s * scale * log2 e - m_new) into P (hi + lo), once the previous P.V is done
-      if (!wait_all(&tl->p_empty, (t & 1) ^ 1)) { ok = false; break; }
+      // pass 2: p = 2^(s * scale * log2 e - m_new), written back over the S
+      // columns just read as hi / lo storage-type pairs (see issue_pv)
       float ls = 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         float sv[32];
         tmem_ld32(sadr + c0, sv);
 #pragma unroll
-        for (int c8 = 0; c8 < 32; c8 += 8) {     // 8 keys = one 16-byte chunk of the row
-          uint32_t hi[4], lo[4];
+        for (int g = 0; g < 32; g += 16) {     // one 16-key group: 8 hi words, 8 lo words
+          uint32_t pw[16];
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            float pa_ = ex2_approx(fmaf(sv[c8 + e], sl2, neg_m));
-            float pb_ = ex2_approx(fmaf(sv[c8 + e + 1], sl2, neg_m));
+          for (int e = 0; e < 16; e += 2) {
+            float pa_ = ex2_approx(fmaf(sv[g + e], sl2, neg_m));
+            float pb_ = ex2_approx(fmaf(sv[g + e + 1], sl2, neg_m));
             if (partial) {
-              pa_ = kc + c0 + c8 + e <= pos ? pa_ : 0.f;
-              pb_ = kc + c0 + c8 + e + 1 <= pos ? pb_ : 0.f;
+              pa_ = kc + c0 + g + e <= pos ? pa_ : 0.f;
+              pb_ = kc + c0 + g + e + 1 <= pos ? pb_ : 0.f;
             }
             ls += pa_ + pb_;
             const uint32_t h2 = narrow2<DT>(pa_, pb_);
             const float2 hf = widen2<DT>(h2);
-            hi[e >> 1] = h2;
-            lo[e >> 1] = narrow2<DT>(pa_ - hf.x, pb_ - hf.y);
+            pw[e >> 1] = h2;
+            pw[8 + (e >> 1)] = narrow2<DT>(pa_ - hf.x, pb_ - hf.y);
           }
-          const int off = ((((c0 + c8) >> 3) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(prow + kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          tmem_st16(sadr + c0 + g, pw);         // over S columns already read
         }
       }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tl->s_empty[sb]);
       l_run = fmaf(l_run, alpha, ls);
       m_run = m_new;
       // keys at or past L: their V rows hold whatever the slot or an earlier tile
