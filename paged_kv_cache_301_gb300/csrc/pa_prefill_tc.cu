@@ -12,18 +12,22 @@
 // TQ = 128 / G query tokens x the G query heads of h (row = token * G + g), so a
 // loaded K/V tile serves all heads of its group.  For KV tiles of 128 keys:
 //
-//   S = Q_tile[128 x D] . K_tile^T            (TMEM, 128 fp32 columns, 2 buffers)
-//   row r: mask keys past its position, running max m, p = exp2(s - m)
-//   P     [128 x 128 keys] as two storage-type terms hi + lo, written to tensor
-//         memory over the S columns it replaces
-//   O_t   = P . V_tile   [128 x D]             (P from TMEM, V from shared memory;
-//                                              TMEM, 2 buffers)
-//   acc  <- acc * exp2(m_old - m_new) + O_t    (registers: thread r owns row r)
+//   S   = Q_tile[128 x D] . K_tile^T           (TMEM, 128 fp32 columns, 2 buffers)
+//   row r: mask keys past its position, running max m, p = 2^(s - m)
+//   P   [128 x 128 keys] as two storage-type terms hi + lo, written to tensor
+//       memory over the S columns it replaces
+//   O  += P . V_tile   [128 x D]               (P from TMEM, V from shared memory,
+//                                              O accumulated in TMEM)
 //
-// Roles (320 threads): warp 0 issues TMA (Q once, then K(t) before V(t-1) into a
-// ring of 32 KB stages), warp 1 issues tcgen05.mma, warps 2-9 run the softmax
-// and own the output rows, two warps per row (64 keys and 64 output columns
-// each).  Every wait is bounded.
+// The running max is raised only when a tile's max exceeds it by more than 8
+// (a factor 2^8): then O (in TMEM) and the row sum are rescaled by
+// 2^(m_old - m_new) before the tile's product; otherwise p may reach 2^8, which
+// fp32 sums and the hi + lo terms carry exactly as well.  The final division by
+// the row sum makes the result independent of which max was used.
+//
+// Roles (576 threads): warp 0 issues TMA (Q once, then K(t) before V(t-1) into a
+// ring of 32 KB stages), warp 1 issues tcgen05.mma, warps 2-17 run the softmax,
+// four warps per row (32 keys and 32 output columns each).  Every wait is bounded.
 #include <math_constants.h>
 
 #include <mutex>
@@ -43,14 +47,16 @@ constexpr int kSlab = 128 * 128;            // 128 rows x 128 bytes
 constexpr int kTile = 2 * kSlab;            // 128 rows x 256 bytes (D = 128, 16-bit)
 constexpr int kQOff = 0;
 constexpr int kRingOff = kQOff + kTile;
-constexpr int kThreads = 320;                // producer, MMA, 8 softmax warps
+constexpr int kSoftWarps = 16;               // four per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kSoftWarps;  // producer, MMA, softmax
+constexpr float kRescaleLog2 = 8.f;          // raise the running max only past this
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kSmemBudget = 232448 - 1024;  // per-block limit minus alignment slack
-constexpr int kTailBytes = 4096;
+constexpr int kTailBytes = 8192;
 constexpr int kStages = (kSmemBudget - kRingOff - kTailBytes) / kTile > 6
                             ? 6 : (kSmemBudget - kRingOff - kTailBytes) / kTile;
 // TMEM: S/P[2] at columns 0 / 128 (P overwrites the S it was computed from),
-// O[2] at 256 / 384
+// O at 256 (allocation is a power of two)
 constexpr uint32_t kTmemCols = 512;
 
 struct Tail {
@@ -58,11 +64,11 @@ struct Tail {
   uint64_t q_full;
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full;
-  uint64_t o_full[2], o_empty[2];
+  uint64_t pv_done;
   uint64_t drain;
-  uint64_t red_bar[2][4], sum_bar[4];          // the two warps of a lane quarter
-  float red_max[2][2][128];                    // [tile parity][half][row]
-  float red_sum[2][128];
+  uint64_t red_bar[2][4], sum_bar[4];          // the four warps of a lane quarter
+  float red_max[2][4][128];                    // [tile parity][column quarter][row]
+  float red_sum[4][128];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -103,8 +109,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
   allow_next_grid();
   wait_prior_grid();               // q, the pools and the tables may come from the previous kernel
-  const int b = blockIdx.x / p.Hkv, h = blockIdx.x - b * p.Hkv;
-  const int qt = p.n_qtiles - 1 - (int)blockIdx.y;     // longest causal work first
+  // blockIdx.x walks the query tiles of one (sequence, KV head), longest causal
+  // work first, so the CTAs resident together read the same K/V from L2
+  const int b = blockIdx.y / p.Hkv, h = blockIdx.y - b * p.Hkv;
+  const int qt = p.n_qtiles - 1 - (int)blockIdx.x;
   const int qs = p.q_start[b];
   const int n = p.q_start[b + 1] - qs;
   const int L = p.seq_lens[b];
@@ -128,12 +136,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tl->s_full[i], 1);
       mbar_init(&tl->s_empty[i], 1);
-      mbar_init(&tl->o_full[i], 1);
-      mbar_init(&tl->o_empty[i], 8);
-      for (int w = 0; w < 4; ++w) mbar_init(&tl->red_bar[i][w], 2);
+      for (int w = 0; w < 4; ++w) mbar_init(&tl->red_bar[i][w], 4);
     }
-    for (int w = 0; w < 4; ++w) mbar_init(&tl->sum_bar[w], 2);
-    mbar_init(&tl->p_full, 8);
+    for (int w = 0; w < 4; ++w) mbar_init(&tl->sum_bar[w], 4);
+    mbar_init(&tl->p_full, kSoftWarps);
+    mbar_init(&tl->pv_done, 1);
     mbar_init(&tl->drain, 1);
     tl->abort_flag = 0;
     fence_mbar_init();
@@ -221,13 +228,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const uint32_t ring = smem_addr(smem + kRingOff);
     const uint32_t qaddr = smem_addr(smem + kQOff);
     bool ok = true, committed = false;
-    // O_u = (P_hi + P_lo) . V_u into O buffer u & 1.  P sits in S buffer u & 1:
-    // 16-key group k occupies columns 16k .. 16k+7 (hi) and 16k+8 .. 16k+15 (lo).
+    // O += (P_hi + P_lo) . V_u.  P sits in S buffer u & 1: 16-key group k occupies
+    // columns 16k .. 16k+7 (hi) and 16k+8 .. 16k+15 (lo).
     auto issue_pv = [&](int u) -> bool {
       const int vs = pos_v(u, last) % kStages, vph = (pos_v(u, last) / kStages) & 1;
       if (!mbar_wait(&tl->full[vs], vph, abort_flag, kWaitNs)) return false;
       if (!mbar_wait(&tl->p_full, u & 1, abort_flag, kWaitNs)) return false;
-      if (!mbar_wait(&tl->o_empty[u & 1], ((u >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
       tc_fence_after();
       const uint32_t vaddr = ring + vs * kTile;
       const uint32_t pcol = tmem + (u & 1) * kKeys;
@@ -236,12 +242,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, kSlab, 1024);
 #pragma unroll
         for (int term = 0; term < 2; ++term)
-          mma_f16_ts(tmem + 256 + (u & 1) * kD, pcol + kk * 16 + term * 8, bd, idesc_o,
-                     (kk | term) != 0);
+          mma_f16_ts(tmem + 256, pcol + kk * 16 + term * 8, bd, idesc_o, (u | kk | term) != 0);
       }
       mma_commit(&tl->empty[vs]);
-      mma_commit(&tl->o_full[u & 1]);
       mma_commit(&tl->s_empty[u & 1]);      // S/P buffer free for S(u + 2)
+      mma_commit(&tl->pv_done);
       return true;
     };
     if (lane == 0) {
@@ -275,40 +280,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
   else {
     // ------------------------------------------------ softmax and output rows --
-    // Two warps per TMEM lane quarter: `half` 0 takes keys 0-63 of each S tile and
-    // columns 0-63 of O, half 1 the other 64; they exchange row maxima per tile.
+    // Four warps per TMEM lane quarter; column quarter j takes keys 32j .. 32j+31
+    // of each S tile and output columns 32j .. 32j+31; the four exchange row maxima.
     const int wq = warp & 3;                     // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;
+    const int j = (warp - 2) >> 2;               // column quarter
     const int r = wq * 32 + lane;                // tile row = query token r / G, head r % G
-    const int cb = half * 64;                    // this thread's first key / O column
+    const int cb = j * 32;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const int i = q0 + r / G;                    // query token within the sequence's queries
     const bool row_valid = i < n;
     const int pos = row_valid ? L - n + i : -1;  // keys 0 .. pos are visible
-    float m_run = -CUDART_INF_F, l_run = 0.f, alpha_prev = 1.f;
-    float acc[64];
-#pragma unroll
-    for (int d = 0; d < 64; ++d) acc[d] = 0.f;
+    const uint32_t ocol = tmem + lane_base + 256 + cb;
+    float m_run = -CUDART_INF_F, l_run = 0.f;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, int parity) -> bool {
       const bool w = mbar_wait(bar, parity, abort_flag, kWaitNs);
       return __all_sync(0xFFFFFFFFu, w);
-    };
-    // acc <- acc * alpha + O_u (this thread's 64 columns)
-    auto accumulate = [&](int u, float alpha) -> bool {
-      if (!wait_all(&tl->o_full[u & 1], (u >> 1) & 1)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        float o[32];
-        tmem_ld32(tmem + lane_base + 256 + (u & 1) * kD + cb + c0, o);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[c0 + e] = fmaf(acc[c0 + e], alpha, o[e]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tl->o_empty[u & 1]);
-      return true;
     };
     const float sl2 = p.scale_log2;
     for (int t = 0; t <= last && ok; ++t) {
@@ -316,63 +303,79 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (!wait_all(&tl->s_full[sb], (t >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
       const int kc = t * kKeys + cb;             // key of this thread's first column
-      const bool partial = kc + 63 > pos;        // some of its keys lie past the row
+      const bool partial = kc + 31 > pos;        // some of its keys lie past the row
       const uint32_t sadr = tmem + lane_base + sb * kKeys + cb;
-      // pass 1: maximum of the visible raw scores (scale > 0 commutes with max)
+      float sv[32];
+      tmem_ld32(sadr, sv);
+      // the tile's maximum of the visible raw scores (scale > 0 commutes with max)
       float mt = -CUDART_INF_F;
+      if (!partial) {
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        float sv[32];
-        tmem_ld32(sadr + c0, sv);
-        if (!partial) {
+        for (int e = 0; e < 32; ++e) mt = fmaxf(mt, sv[e]);
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, sv[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, kc + c0 + e <= pos ? sv[e] : -CUDART_INF_F);
-        }
+        for (int e = 0; e < 32; ++e) mt = fmaxf(mt, kc + e <= pos ? sv[e] : -CUDART_INF_F);
       }
-      {   // row maximum over both halves
+      {   // over the row's four column quarters
         const int rb = t & 1;
-        tl->red_max[rb][half][r] = mt;
+        tl->red_max[rb][j][r] = mt;
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->red_bar[rb][wq]);
         if (!wait_all(&tl->red_bar[rb][wq], (t >> 1) & 1)) { ok = false; break; }
-        mt = fmaxf(mt, tl->red_max[rb][half ^ 1][r]);
+        mt = fmaxf(fmaxf(tl->red_max[rb][0][r], tl->red_max[rb][1][r]),
+                   fmaxf(tl->red_max[rb][2][r], tl->red_max[rb][3][r]));
       }
-      const float m_new = fmaxf(m_run, mt * sl2);
-      const float alpha = m_new == -CUDART_INF_F ? 1.f : ex2_approx(m_run - m_new);
-      const float neg_m = m_new == -CUDART_INF_F ? 0.f : -m_new;
-      // pass 2: p = 2^(s * scale * log2 e - m_new), written back over the S
-      // columns just read as hi / lo storage-type pairs (see issue_pv)
+      const float m_tile = mt * sl2;
+      // Rows whose max grows by more than 2^8 raise it; O (complete up to tile
+      // t-1) and l scale by 2^(m_old - m_new).  TMEM access is warp-wide, so the
+      // warp rescales when any of its rows needs it (the others by 1).
+      const bool raise = m_run != -CUDART_INF_F && m_tile > m_run + kRescaleLog2;
+      if (__any_sync(0xFFFFFFFFu, raise)) {
+        const float alpha = raise ? ex2_approx(m_run - m_tile) : 1.f;
+        if (!wait_all(&tl->pv_done, (t - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        float o[32];
+        tmem_ld32(ocol, o);
+        uint32_t ow[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ow[e] = __float_as_uint(o[e] * alpha);
+        tmem_st32(ocol, ow);
+        l_run *= alpha;
+      }
+      if (m_run == -CUDART_INF_F || raise) m_run = m_tile;   // first visible tile, or raised
+      const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
+      // p = 2^(s * scale * log2 e - m), written back over the S columns as
+      // hi / lo storage-type pairs (see issue_pv)
       float ls = 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        float sv[32];
-        tmem_ld32(sadr + c0, sv);
+      for (int g = 0; g < 32; g += 16) {         // one 16-key group: 8 hi words, 8 lo words
+        uint32_t pw[16];
 #pragma unroll
-        for (int g = 0; g < 32; g += 16) {     // one 16-key group: 8 hi words, 8 lo words
-          uint32_t pw[16];
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            float pa_ = ex2_approx(fmaf(sv[g + e], sl2, neg_m));
-            float pb_ = ex2_approx(fmaf(sv[g + e + 1], sl2, neg_m));
-            if (partial) {
-              pa_ = kc + c0 + g + e <= pos ? pa_ : 0.f;
-              pb_ = kc + c0 + g + e + 1 <= pos ? pb_ : 0.f;
-            }
-            ls += pa_ + pb_;
+        for (int e = 0; e < 16; e += 2) {
+          float pa_ = ex2_approx(fmaf(sv[g + e], sl2, neg_m));
+          float pb_ = ex2_approx(fmaf(sv[g + e + 1], sl2, neg_m));
+          if (partial) {
+            pa_ = kc + g + e <= pos ? pa_ : 0.f;
+            pb_ = kc + g + e + 1 <= pos ? pb_ : 0.f;
+          }
+          ls += pa_ + pb_;
+          if (DT == PA_BFLOAT16) {
+            // hi = the top 16 bits (truncation), lo = the rest rounded: hi + lo
+            // carries ~16 significant bits either way
+            const uint32_t ua = __float_as_uint(pa_), ub = __float_as_uint(pb_);
+            pw[e >> 1] = __byte_perm(ua, ub, 0x7632);
+            pw[8 + (e >> 1)] = narrow2<DT>(pa_ - __uint_as_float(ua & 0xFFFF0000u),
+                                           pb_ - __uint_as_float(ub & 0xFFFF0000u));
+          } else {
             const uint32_t h2 = narrow2<DT>(pa_, pb_);
             const float2 hf = widen2<DT>(h2);
             pw[e >> 1] = h2;
             pw[8 + (e >> 1)] = narrow2<DT>(pa_ - hf.x, pb_ - hf.y);
           }
-          tmem_st16(sadr + c0 + g, pw);         // over S columns already read
         }
+        tmem_st16(sadr + g, pw);                 // over S columns already read
       }
-      tc_fence_before();
-      l_run = fmaf(l_run, alpha, ls);
-      m_run = m_new;
+      l_run += ls;
       // keys at or past L: their V rows hold whatever the slot or an earlier tile
       // left (0 * NaN must not reach O), so zero them before P.V reads the tile
       const int k0 = t * kKeys;
@@ -380,37 +383,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int u = pos_v(t, last);
         const int vs = u % kStages, vph = (u / kStages) & 1;
         if (!wait_all(&tl->full[vs], vph)) { ok = false; break; }
-        if (k0 + r >= L) {
-          uint4* v0 = reinterpret_cast<uint4*>(smem + kRingOff + vs * kTile + half * kSlab + r * 128);
+        if (k0 + r >= L) {                       // V row r: this warp zeroes 32 of its 128 columns
+          uint4* v0 = reinterpret_cast<uint4*>(smem + kRingOff + vs * kTile + (j >> 1) * kSlab +
+                                               r * 128 + (j & 1) * 64);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v0[e] = make_uint4(0, 0, 0, 0);
+          for (int e = 0; e < 4; ++e) v0[e] = make_uint4(0, 0, 0, 0);
         }
       }
+      // consume P.V(t-1)'s completion before P(t) is released, so the barrier
+      // cannot run two phases ahead of any waiting warp
+      if (t > 0 && !wait_all(&tl->pv_done, (t - 1) & 1)) { ok = false; break; }
+      tc_fence_before();
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tl->p_full);
-      if (t > 0 && !accumulate(t - 1, alpha_prev)) { ok = false; break; }
-      alpha_prev = alpha;
     }
-    if (ok) ok = accumulate(last, alpha_prev);
-    if (ok) {   // row sum over both halves
-      tl->red_sum[half][r] = l_run;
+    if (ok) ok = wait_all(&tl->pv_done, last & 1);
+    if (ok) {   // row sum over the four column quarters
+      tl->red_sum[j][r] = l_run;
       __syncwarp();
       if (lane == 0) mbar_arrive(&tl->sum_bar[wq]);
       ok = wait_all(&tl->sum_bar[wq], 0);
     }
     if (!ok) {
       if (lane == 0) set_abort();
-    } else if (row_valid) {
-      const float inv = 1.f / (l_run + tl->red_sum[half ^ 1][r]);
-      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                          ((int64_t)(qs + i) * p.Hq + h * G + r % G) * kD + cb);
+    } else {
+      tc_fence_after();
+      float o[32];
+      tmem_ld32(ocol, o);
+      if (row_valid) {
+        const float inv = 1.f / (tl->red_sum[0][r] + tl->red_sum[1][r] + tl->red_sum[2][r] +
+                                 tl->red_sum[3][r]);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                              ((int64_t)(qs + i) * p.Hq + h * G + r % G) * kD + cb);
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        o[c] = make_uint4(narrow2<DT>(acc[8 * c] * inv, acc[8 * c + 1] * inv),
-                          narrow2<DT>(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv),
-                          narrow2<DT>(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv),
-                          narrow2<DT>(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv));
+        for (int c = 0; c < 4; ++c)
+          dst[c] = make_uint4(narrow2<DT>(o[8 * c] * inv, o[8 * c + 1] * inv),
+                              narrow2<DT>(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                              narrow2<DT>(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                              narrow2<DT>(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+      }
     }
   }
 
@@ -451,7 +463,7 @@ pa_status launch_g(const PrefillParams& p, const CUtensorMap& k, const CUtensorM
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr != cudaSuccess) return PA_ERR_CUDA;
-  const dim3 grid((unsigned)(p.Hkv * p.B), (unsigned)p.n_qtiles);
+  const dim3 grid((unsigned)p.n_qtiles, (unsigned)(p.Hkv * p.B));
   if (launch_pdl(prefill_tc_kernel<DT, G>, grid, kThreads, kSmemBytes, stream, k, v, q, p) !=
       cudaSuccess)
     return PA_ERR_CUDA;
@@ -499,12 +511,11 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
     return PA_ERR_INVALID_ARG;
   if ((int64_t)num_blocks * block_size >= (1ll << 31) ||
-      (int64_t)num_seqs * num_kv_heads >= (1ll << 31) ||
       (int64_t)total_q * num_q_heads >= (1ll << 31))
     return PA_ERR_INVALID_ARG;
   const int TQ = kRows / G;
   const int64_t n_qtiles = ((int64_t)max_q_len + TQ - 1) / TQ;
-  if (n_qtiles > 65535) return PA_ERR_INVALID_ARG;
+  if ((int64_t)num_seqs * num_kv_heads > 65535) return PA_ERR_INVALID_ARG;   // grid y
   EncodeTiledFn enc = encode_fn();
   if (!enc) return PA_ERR_UNSUPPORTED;
 
