@@ -8,26 +8,31 @@
 // Attention" §5 "The kernel side" for many queries, each limited to the
 // positions up to its own.
 //
-// Work item (one CTA): sequence b, KV head h, query tile of 128 rows =
-// TQ = 128 / G query tokens x the G query heads of h (row = token * G + g), so a
-// loaded K/V tile serves all heads of its group.  For KV tiles of 128 keys:
+// Work item (one CTA): sequence b, KV head h and two adjacent query tiles A, B
+// of 128 rows each = TQ = 128 / G query tokens x the G query heads of h
+// (row = token * G + g).  Every K/V tile loaded serves both, 256 query rows, so
+// the per-head gather (128-byte rows 2 KB apart, ~35 GB/s per SM through TMA on
+// GB300) feeds twice the tensor work of a single tile.  For KV tiles of 128 keys
+// and each query tile k:
 //
-//   S   = Q_tile[128 x D] . K_tile^T           (TMEM, 128 fp32 columns, 2 buffers)
+//   S_k  = Q_k[128 x D] . K_tile^T           (TMEM, 128 fp32 columns)
 //   row r: mask keys past its position, running max m, p = 2^(s - m)
-//   P   [128 x 128 keys] as two storage-type terms hi + lo, written to tensor
-//       memory over the S columns it replaces
-//   O  += P . V_tile   [128 x D]               (P from TMEM, V from shared memory,
-//                                              O accumulated in TMEM)
+//   P_k  [128 x 128 keys] as two storage-type terms hi + lo, written to tensor
+//        memory over the S columns it replaces
+//   O_k += P_k . V_tile   [128 x D]          (P from TMEM, V from shared memory,
+//                                             O accumulated in TMEM)
 //
-// The running max is raised only when a tile's max exceeds it by more than 8
-// (a factor 2^8): then O (in TMEM) and the row sum are rescaled by
-// 2^(m_old - m_new) before the tile's product; otherwise p may reach 2^8, which
-// fp32 sums and the hi + lo terms carry exactly as well.  The final division by
-// the row sum makes the result independent of which max was used.
+// The tensor core alternates between the tiles (P_A.V, S_A next, P_B.V, S_B
+// next) while the softmax warps of the other tile work.  The running max is
+// raised only when a tile's max exceeds it by more than 8 (a factor 2^8): O and
+// the row sum are then rescaled by 2^(m_old - m_new) before the tile's product;
+// otherwise p may reach 2^8, which fp32 sums and the hi + lo terms carry as
+// well.  The final division by the row sum removes the choice of max.
 //
-// Roles (576 threads): warp 0 issues TMA (Q once, then K(t) before V(t-1) into a
-// ring of 32 KB stages), warp 1 issues tcgen05.mma, warps 2-17 run the softmax,
-// four warps per row (32 keys and 32 output columns each).  Every wait is bounded.
+// Roles (576 threads): warp 0 issues TMA (both Q tiles, then K(t), V(t) into a
+// ring of 32 KB stages), warp 1 issues tcgen05.mma, warps 2-9 run tile A's
+// softmax and warps 10-17 tile B's, two warps per row (64 keys and 64 output
+// columns each).  Every wait is bounded.
 #include <math_constants.h>
 
 #include <mutex>
@@ -45,30 +50,28 @@ constexpr int kRows = 128;                  // query rows per tile (M)
 constexpr int kKeys = 128;                  // keys per KV tile (N of S, K of P.V)
 constexpr int kSlab = 128 * 128;            // 128 rows x 128 bytes
 constexpr int kTile = 2 * kSlab;            // 128 rows x 256 bytes (D = 128, 16-bit)
-constexpr int kQOff = 0;
-constexpr int kRingOff = kQOff + kTile;
-constexpr int kSoftWarps = 16;               // four per TMEM lane quarter
-constexpr int kThreads = 64 + 32 * kSoftWarps;  // producer, MMA, softmax
-constexpr float kRescaleLog2 = 8.f;          // raise the running max only past this
+constexpr int kQOff = 0;                    // Q_A, then Q_B
+constexpr int kRingOff = kQOff + 2 * kTile;
+constexpr int kSoftWarps = 16;              // eight per query tile
+constexpr int kThreads = 64 + 32 * kSoftWarps;
+constexpr float kRescaleLog2 = 8.f;         // raise the running max only past this
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kSmemBudget = 232448 - 1024;  // per-block limit minus alignment slack
 constexpr int kTailBytes = 8192;
 constexpr int kStages = (kSmemBudget - kRingOff - kTailBytes) / kTile > 6
                             ? 6 : (kSmemBudget - kRingOff - kTailBytes) / kTile;
-// TMEM: S/P[2] at columns 0 / 128 (P overwrites the S it was computed from),
-// O at 256 (allocation is a power of two)
+// TMEM: S/P_A at column 0, S/P_B at 128 (P overwrites the S it was computed
+// from), O_A at 256, O_B at 384
 constexpr uint32_t kTmemCols = 512;
 
 struct Tail {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full;
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full;
-  uint64_t pv_done;
+  uint64_t s_full[2], p_full[2], pv_done[2];   // per query tile
+  uint64_t red_bar[2][2][4], sum_bar[2][4];    // [tile][parity][lane quarter]
   uint64_t drain;
-  uint64_t red_bar[2][4], sum_bar[4];          // the four warps of a lane quarter
-  float red_max[2][4][128];                    // [tile parity][column quarter][row]
-  float red_sum[4][128];
+  float red_max[2][2][2][128];                 // [tile][parity][half][row]
+  float red_sum[2][2][128];                    // [tile][half][row]
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -83,16 +86,10 @@ struct PrefillParams {
   const int32_t* tables;        // [B, max_blocks]
   const int32_t* seq_lens;      // [B]
   const int32_t* q_start;       // [B + 1]
-  int B, total_q, Hq, Hkv, bs, max_blocks, num_blocks, max_q_len, n_qtiles;
+  int B, total_q, Hq, Hkv, bs, max_blocks, num_blocks, max_q_len, n_qpairs;
   float scale_log2;
   int32_t* status_dev;
 };
-
-// Ring positions in the MMA's consumption order K(0), K(1), V(0), K(2), V(1), ...,
-// V(last): S(t) is issued before P(t-1).V(t-1) so the softmax of tile t can start
-// while the previous product runs.
-__device__ __forceinline__ int pos_k(int t) { return t == 0 ? 0 : 2 * t - 1; }
-__device__ __forceinline__ int pos_v(int t, int last) { return t < last ? 2 * t + 2 : 2 * t + 1; }
 
 template <int DT, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -109,23 +106,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
   allow_next_grid();
   wait_prior_grid();               // q, the pools and the tables may come from the previous kernel
-  // blockIdx.x walks the query tiles of one (sequence, KV head), longest causal
-  // work first, so the CTAs resident together read the same K/V from L2
+  // blockIdx.x walks the query-tile pairs of one (sequence, KV head), longest
+  // causal work first, so the CTAs resident together read the same K/V from L2
   const int b = blockIdx.y / p.Hkv, h = blockIdx.y - b * p.Hkv;
-  const int qt = p.n_qtiles - 1 - (int)blockIdx.x;
+  const int qp = p.n_qpairs - 1 - (int)blockIdx.x;
   const int qs = p.q_start[b];
   const int n = p.q_start[b + 1] - qs;
   const int L = p.seq_lens[b];
   if (n < 0 || n > L || n > p.max_q_len || L > p.max_blocks * p.bs || qs < 0 ||
       qs + n > p.total_q) {
-    if (threadIdx.x == 0 && h == 0 && qt == 0) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+    if (threadIdx.x == 0 && h == 0 && qp == 0) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
     return;
   }
-  const int q0 = qt * TQ;
-  if (q0 >= n) return;                          // uniform: no rows in this tile
-  const int pos_last = L - n + min(q0 + TQ, n) - 1;
-  const int n_kv = pos_last / kKeys + 1;        // KV tiles covering keys 0 .. pos_last
-  const int last = n_kv - 1;
+  // query tile k = 0 (A), 1 (B): first query token, and the KV tiles 0 .. last_k
+  // its causal rows reach (-1: no rows)
+  const int q0a = 2 * qp * TQ, q0b = q0a + TQ;
+  if (q0a >= n) return;                         // uniform: no rows in this pair
+  const int last_a = (L - n + min(q0a + TQ, n) - 1) / kKeys;
+  const int last_b = q0b < n ? (L - n + min(q0b + TQ, n) - 1) / kKeys : -1;
+  const int last_all = last_b >= 0 ? last_b : last_a;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -133,14 +132,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       mbar_init(&tl->empty[s], 1);
     }
     mbar_init(&tl->q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&tl->s_full[i], 1);
-      mbar_init(&tl->s_empty[i], 1);
-      for (int w = 0; w < 4; ++w) mbar_init(&tl->red_bar[i][w], 4);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&tl->s_full[k], 1);
+      mbar_init(&tl->p_full[k], kSoftWarps / 2);
+      mbar_init(&tl->pv_done[k], 1);
+      for (int w = 0; w < 4; ++w) {
+        mbar_init(&tl->red_bar[k][0][w], 2);
+        mbar_init(&tl->red_bar[k][1][w], 2);
+        mbar_init(&tl->sum_bar[k][w], 2);
+      }
     }
-    for (int w = 0; w < 4; ++w) mbar_init(&tl->sum_bar[w], 4);
-    mbar_init(&tl->p_full, kSoftWarps);
-    mbar_init(&tl->pv_done, 1);
     mbar_init(&tl->drain, 1);
     tl->abort_flag = 0;
     fence_mbar_init();
@@ -175,10 +176,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
     for (int s = 0; s < kStages; ++s) issued[s] = -1;
     bool ok = true, q_issued = false;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&tl->q_full, kTile);
-      tma_load_3d_hint(smem + kQOff, &tm_q, &tl->q_full, 0, h * G, qs + q0, q_policy);
-      tma_load_3d_hint(smem + kQOff + kSlab, &tm_q, &tl->q_full, 64, h * G, qs + q0, q_policy);
+    if (lane == 0) {            // both query tiles (rows past the batch read as zeros)
+      mbar_arrive_expect_tx(&tl->q_full, 2 * kTile);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint8_t* dst = smem + kQOff + k * kTile;
+        const int z = qs + (k ? q0b : q0a);
+        tma_load_3d_hint(dst, &tm_q, &tl->q_full, 0, h * G, z, q_policy);
+        tma_load_3d_hint(dst + kSlab, &tm_q, &tl->q_full, 64, h * G, z, q_policy);
+      }
       q_issued = true;
     }
     // one K or V tile: lanes < nops each copy one block (both 64-column slabs)
@@ -209,18 +215,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       return true;
     };
-    for (int t = 0; t <= last && ok; ++t) {
+    for (int t = 0; t <= last_all && ok; ++t) {      // ring order: K(0), V(0), K(1), V(1), ...
       ok = issue(&tm_k, t);
-      if (ok && t > 0) ok = issue(&tm_v, t - 1);
+      if (ok) ok = issue(&tm_v, t);
     }
-    if (ok) ok = issue(&tm_v, last);
     if (*abort_flag && lane == 0) {            // let copies in flight land before exit
       for (int s = 0; s < kStages; ++s)
         if (issued[s] >= 0) mbar_wait_drain(&tl->full[s], issued[s], kWaitNs);
       if (q_issued) mbar_wait_drain(&tl->q_full, 0, kWaitNs);
     }
-  }
-  else if (warp == 1) {
+  } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issue --
     constexpr uint32_t ab = DT == PA_BFLOAT16 ? 1u : 0u;
     constexpr uint32_t idesc_s = idesc_f16(ab, 0, 0, kRows, kKeys);   // Q, K both K-major
@@ -228,48 +232,67 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const uint32_t ring = smem_addr(smem + kRingOff);
     const uint32_t qaddr = smem_addr(smem + kQOff);
     bool ok = true, committed = false;
-    // O += (P_hi + P_lo) . V_u.  P sits in S buffer u & 1: 16-key group k occupies
-    // columns 16k .. 16k+7 (hi) and 16k+8 .. 16k+15 (lo).
-    auto issue_pv = [&](int u) -> bool {
-      const int vs = pos_v(u, last) % kStages, vph = (pos_v(u, last) / kStages) & 1;
-      if (!mbar_wait(&tl->full[vs], vph, abort_flag, kWaitNs)) return false;
-      if (!mbar_wait(&tl->p_full, u & 1, abort_flag, kWaitNs)) return false;
-      tc_fence_after();
-      const uint32_t vaddr = ring + vs * kTile;
-      const uint32_t pcol = tmem + (u & 1) * kKeys;
+    // S_k = Q_k . K(t)^T into S/P buffer k
+    auto issue_s = [&](int k, int t) {
+      const uint32_t kaddr = ring + ((2 * t) % kStages) * kTile;
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
+        mma_f16(tmem + k * kKeys, smem_desc_sw128(qaddr + k * kTile + off, 16, 1024),
+                smem_desc_sw128(kaddr + off, 16, 1024), idesc_s, kk > 0);
+      }
+      mma_commit(&tl->s_full[k]);
+    };
+    // O_k += (P_hi + P_lo) . V(t).  P sits in S/P buffer k: 16-key group g occupies
+    // columns 16g .. 16g+7 (hi) and 16g+8 .. 16g+15 (lo).
+    auto issue_pv = [&](int k, int t) {
+      const uint32_t vaddr = ring + ((2 * t + 1) % kStages) * kTile;
 #pragma unroll
       for (int kk = 0; kk < kKeys / 16; ++kk) {
         const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, kSlab, 1024);
 #pragma unroll
         for (int term = 0; term < 2; ++term)
-          mma_f16_ts(tmem + 256, pcol + kk * 16 + term * 8, bd, idesc_o, (u | kk | term) != 0);
+          mma_f16_ts(tmem + 256 + k * kD, tmem + k * kKeys + kk * 16 + term * 8, bd, idesc_o,
+                     (t | kk | term) != 0);
       }
-      mma_commit(&tl->empty[vs]);
-      mma_commit(&tl->s_empty[u & 1]);      // S/P buffer free for S(u + 2)
-      mma_commit(&tl->pv_done);
-      return true;
+      mma_commit(&tl->pv_done[k]);
+    };
+    auto stage_wait = [&](int pos) -> bool {
+      return mbar_wait(&tl->full[pos % kStages], (pos / kStages) & 1, abort_flag, kWaitNs);
     };
     if (lane == 0) {
-      ok = mbar_wait(&tl->q_full, 0, abort_flag, kWaitNs);
-      for (int t = 0; t <= last && ok; ++t) {
-        const int ks = pos_k(t) % kStages, kph = (pos_k(t) / kStages) & 1;
-        ok = mbar_wait(&tl->full[ks], kph, abort_flag, kWaitNs) &&
-             mbar_wait(&tl->s_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag, kWaitNs);
-        if (!ok) break;
+      ok = mbar_wait(&tl->q_full, 0, abort_flag, kWaitNs) && stage_wait(0);
+      if (ok) {
         tc_fence_after();
-        const uint32_t kaddr = ring + ks * kTile;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
-          mma_f16(tmem + (t & 1) * kKeys, smem_desc_sw128(qaddr + off, 16, 1024),
-                  smem_desc_sw128(kaddr + off, 16, 1024), idesc_s, kk > 0);
-        }
-        mma_commit(&tl->empty[ks]);
-        mma_commit(&tl->s_full[t & 1]);
+        issue_s(0, 0);
+        if (last_b >= 0) issue_s(1, 0);
+        mma_commit(&tl->empty[0]);
         committed = true;
-        if (t > 0) ok = issue_pv(t - 1);
       }
-      if (ok) ok = issue_pv(last);
+      for (int t = 0; t <= last_all && ok; ++t) {
+        ok = stage_wait(2 * t + 1);                      // V(t)
+        bool next_k = false;                             // K(t+1) landed
+        for (int k = 0; k < 2 && ok; ++k) {
+          const int last_k = k ? last_b : last_a;
+          if (t > last_k) continue;
+          ok = mbar_wait(&tl->p_full[k], t & 1, abort_flag, kWaitNs);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(k, t);
+          if (t + 1 <= last_k) {
+            // S_k(t+1) overwrites P_k(t): after P_k(t).V(t) has read it
+            ok = (next_k || stage_wait(2 * t + 2)) &&
+                 mbar_wait(&tl->pv_done[k], t & 1, abort_flag, kWaitNs);
+            if (!ok) break;
+            next_k = true;
+            tc_fence_after();
+            issue_s(k, t + 1);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tl->empty[(2 * t + 1) % kStages]);   // V(t) read by every product
+        if (t + 1 <= last_all) mma_commit(&tl->empty[(2 * t + 2) % kStages]);   // K(t+1)
+      }
       if (!ok) set_abort();
       if (*abort_flag && committed) {          // let issued MMAs finish before TMEM is freed
         mma_commit(&tl->drain);
@@ -280,50 +303,54 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
   else {
     // ------------------------------------------------ softmax and output rows --
-    // Four warps per TMEM lane quarter; column quarter j takes keys 32j .. 32j+31
-    // of each S tile and output columns 32j .. 32j+31; the four exchange row maxima.
+    // Tile k = 0 (A) or 1 (B); two warps per TMEM lane quarter, half 0 with keys
+    // 0-63 of each S tile and output columns 0-63, half 1 with the rest.
+    const int k = (warp - 2) >> 3;
+    const int half = ((warp - 2) >> 2) & 1;
     const int wq = warp & 3;                     // TMEM lane quarter of this warp
-    const int j = (warp - 2) >> 2;               // column quarter
     const int r = wq * 32 + lane;                // tile row = query token r / G, head r % G
-    const int cb = j * 32;
+    const int cb = half * 64;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const int i = q0 + r / G;                    // query token within the sequence's queries
+    const int i = (k ? q0b : q0a) + r / G;       // query token within the sequence's queries
     const bool row_valid = i < n;
     const int pos = row_valid ? L - n + i : -1;  // keys 0 .. pos are visible
-    const uint32_t ocol = tmem + lane_base + 256 + cb;
+    const uint32_t scol = tmem + lane_base + k * kKeys + cb;
+    const uint32_t ocol = tmem + lane_base + 256 + k * kD + cb;
+    const float sl2 = p.scale_log2;
     float m_run = -CUDART_INF_F, l_run = 0.f;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, int parity) -> bool {
       const bool w = mbar_wait(bar, parity, abort_flag, kWaitNs);
       return __all_sync(0xFFFFFFFFu, w);
     };
-    const float sl2 = p.scale_log2;
-    for (int t = 0; t <= last && ok; ++t) {
-      const int sb = t & 1;
-      if (!wait_all(&tl->s_full[sb], (t >> 1) & 1)) { ok = false; break; }
+    const int my_last = k ? last_b : last_a;
+    for (int t = 0; t <= my_last && ok; ++t) {
+      if (!wait_all(&tl->s_full[k], t & 1)) { ok = false; break; }
       tc_fence_after();
       const int kc = t * kKeys + cb;             // key of this thread's first column
-      const bool partial = kc + 31 > pos;        // some of its keys lie past the row
-      const uint32_t sadr = tmem + lane_base + sb * kKeys + cb;
-      float sv[32];
-      tmem_ld32(sadr, sv);
-      // the tile's maximum of the visible raw scores (scale > 0 commutes with max)
+      const bool partial = kc + 63 > pos;        // some of its keys lie past the row
+      // the tile's maximum of the visible raw scores (scale > 0 commutes with max);
+      // S is read again for the exponentials (registers hold one 32-column chunk)
       float mt = -CUDART_INF_F;
-      if (!partial) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mt = fmaxf(mt, sv[e]);
-      } else {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        float sv[32];
+        tmem_ld32(scol + c0, sv);
+        if (!partial) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mt = fmaxf(mt, kc + e <= pos ? sv[e] : -CUDART_INF_F);
+          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, sv[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, kc + c0 + e <= pos ? sv[e] : -CUDART_INF_F);
+        }
       }
-      {   // over the row's four column quarters
+      {   // over the row's two halves
         const int rb = t & 1;
-        tl->red_max[rb][j][r] = mt;
+        tl->red_max[k][rb][half][r] = mt;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->red_bar[rb][wq]);
-        if (!wait_all(&tl->red_bar[rb][wq], (t >> 1) & 1)) { ok = false; break; }
-        mt = fmaxf(fmaxf(tl->red_max[rb][0][r], tl->red_max[rb][1][r]),
-                   fmaxf(tl->red_max[rb][2][r], tl->red_max[rb][3][r]));
+        if (lane == 0) mbar_arrive(&tl->red_bar[k][rb][wq]);
+        if (!wait_all(&tl->red_bar[k][rb][wq], (t >> 1) & 1)) { ok = false; break; }
+        mt = fmaxf(mt, tl->red_max[k][rb][half ^ 1][r]);
       }
       const float m_tile = mt * sl2;
       // Rows whose max grows by more than 2^8 raise it; O (complete up to tile
@@ -332,96 +359,109 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       const bool raise = m_run != -CUDART_INF_F && m_tile > m_run + kRescaleLog2;
       if (__any_sync(0xFFFFFFFFu, raise)) {
         const float alpha = raise ? ex2_approx(m_run - m_tile) : 1.f;
-        if (!wait_all(&tl->pv_done, (t - 1) & 1)) { ok = false; break; }
+        if (!wait_all(&tl->pv_done[k], (t - 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        float o[32];
-        tmem_ld32(ocol, o);
-        uint32_t ow[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) ow[e] = __float_as_uint(o[e] * alpha);
-        tmem_st32(ocol, ow);
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          float o[32];
+          tmem_ld32(ocol + c0, o);
+          uint32_t ow[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ow[e] = __float_as_uint(o[e] * alpha);
+          tmem_st32(ocol + c0, ow);
+        }
         l_run *= alpha;
       }
       if (m_run == -CUDART_INF_F || raise) m_run = m_tile;   // first visible tile, or raised
       const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
       // p = 2^(s * scale * log2 e - m), written back over the S columns as
-      // hi / lo storage-type pairs (see issue_pv)
+      // hi / lo storage-type pairs (16-key group: 8 hi words, then 8 lo words)
       float ls = 0.f;
 #pragma unroll
-      for (int g = 0; g < 32; g += 16) {         // one 16-key group: 8 hi words, 8 lo words
-        uint32_t pw[16];
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        float sv[32];
+        tmem_ld32(scol + c0, sv);
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float pa_ = ex2_approx(fmaf(sv[g + e], sl2, neg_m));
-          float pb_ = ex2_approx(fmaf(sv[g + e + 1], sl2, neg_m));
-          if (partial) {
-            pa_ = kc + g + e <= pos ? pa_ : 0.f;
-            pb_ = kc + g + e + 1 <= pos ? pb_ : 0.f;
+        for (int g = 0; g < 32; g += 16) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            float pa_ = ex2_approx(fmaf(sv[g + e], sl2, neg_m));
+            float pb_ = ex2_approx(fmaf(sv[g + e + 1], sl2, neg_m));
+            if (partial) {
+              pa_ = kc + c0 + g + e <= pos ? pa_ : 0.f;
+              pb_ = kc + c0 + g + e + 1 <= pos ? pb_ : 0.f;
+            }
+            ls += pa_ + pb_;
+            if (DT == PA_BFLOAT16) {
+              // hi = the top 16 bits (truncation), lo = the rest rounded: hi + lo
+              // carries ~16 significant bits either way
+              const uint32_t ua = __float_as_uint(pa_), ub = __float_as_uint(pb_);
+              pw[e >> 1] = __byte_perm(ua, ub, 0x7632);
+              pw[8 + (e >> 1)] = narrow2<DT>(pa_ - __uint_as_float(ua & 0xFFFF0000u),
+                                             pb_ - __uint_as_float(ub & 0xFFFF0000u));
+            } else {
+              const uint32_t h2 = narrow2<DT>(pa_, pb_);
+              const float2 hf = widen2<DT>(h2);
+              pw[e >> 1] = h2;
+              pw[8 + (e >> 1)] = narrow2<DT>(pa_ - hf.x, pb_ - hf.y);
+            }
           }
-          ls += pa_ + pb_;
-          if (DT == PA_BFLOAT16) {
-            // hi = the top 16 bits (truncation), lo = the rest rounded: hi + lo
-            // carries ~16 significant bits either way
-            const uint32_t ua = __float_as_uint(pa_), ub = __float_as_uint(pb_);
-            pw[e >> 1] = __byte_perm(ua, ub, 0x7632);
-            pw[8 + (e >> 1)] = narrow2<DT>(pa_ - __uint_as_float(ua & 0xFFFF0000u),
-                                           pb_ - __uint_as_float(ub & 0xFFFF0000u));
-          } else {
-            const uint32_t h2 = narrow2<DT>(pa_, pb_);
-            const float2 hf = widen2<DT>(h2);
-            pw[e >> 1] = h2;
-            pw[8 + (e >> 1)] = narrow2<DT>(pa_ - hf.x, pb_ - hf.y);
-          }
+          tmem_st16(scol + c0 + g, pw);          // over S columns already read
         }
-        tmem_st16(sadr + g, pw);                 // over S columns already read
       }
       l_run += ls;
       // keys at or past L: their V rows hold whatever the slot or an earlier tile
-      // left (0 * NaN must not reach O), so zero them before P.V reads the tile
+      // left (0 * NaN must not reach O).  The first tile whose product reads V(t)
+      // zeroes them before releasing its P.
       const int k0 = t * kKeys;
-      if (k0 + kKeys > L) {
-        const int u = pos_v(t, last);
-        const int vs = u % kStages, vph = (u / kStages) & 1;
-        if (!wait_all(&tl->full[vs], vph)) { ok = false; break; }
-        if (k0 + r >= L) {                       // V row r: this warp zeroes 32 of its 128 columns
-          uint4* v0 = reinterpret_cast<uint4*>(smem + kRingOff + vs * kTile + (j >> 1) * kSlab +
-                                               r * 128 + (j & 1) * 64);
+      if (k0 + kKeys > L && (k == 0 || t > last_a)) {
+        const int u = 2 * t + 1;
+        if (!wait_all(&tl->full[u % kStages], (u / kStages) & 1)) { ok = false; break; }
+        if (k0 + r >= L) {                       // V row r: this warp zeroes one 64-column slab
+          uint4* v0 = reinterpret_cast<uint4*>(smem + kRingOff + (u % kStages) * kTile +
+                                               half * kSlab + r * 128);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) v0[e] = make_uint4(0, 0, 0, 0);
+          for (int e = 0; e < 8; ++e) v0[e] = make_uint4(0, 0, 0, 0);
         }
       }
       // consume P.V(t-1)'s completion before P(t) is released, so the barrier
       // cannot run two phases ahead of any waiting warp
-      if (t > 0 && !wait_all(&tl->pv_done, (t - 1) & 1)) { ok = false; break; }
+      if (t > 0 && !wait_all(&tl->pv_done[k], (t - 1) & 1)) { ok = false; break; }
       tc_fence_before();
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tl->p_full);
+      if (lane == 0) mbar_arrive(&tl->p_full[k]);
     }
-    if (ok) ok = wait_all(&tl->pv_done, last & 1);
-    if (ok) {   // row sum over the four column quarters
-      tl->red_sum[j][r] = l_run;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tl->sum_bar[wq]);
-      ok = wait_all(&tl->sum_bar[wq], 0);
-    }
-    if (!ok) {
-      if (lane == 0) set_abort();
-    } else {
-      tc_fence_after();
-      float o[32];
-      tmem_ld32(ocol, o);
-      if (row_valid) {
-        const float inv = 1.f / (tl->red_sum[0][r] + tl->red_sum[1][r] + tl->red_sum[2][r] +
-                                 tl->red_sum[3][r]);
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                              ((int64_t)(qs + i) * p.Hq + h * G + r % G) * kD + cb);
+    if (my_last >= 0) {
+      if (ok) ok = wait_all(&tl->pv_done[k], my_last & 1);
+      if (ok) {   // row sum over both halves
+        tl->red_sum[k][half][r] = l_run;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->sum_bar[k][wq]);
+        ok = wait_all(&tl->sum_bar[k][wq], 0);
+      }
+      if (!ok) {
+        if (lane == 0) set_abort();
+      } else {
+        tc_fence_after();
+        const float inv = 1.f / (l_run + tl->red_sum[k][half ^ 1][r]);
+        uint4* dst = reinterpret_cast<uint4*>(
+            static_cast<uint16_t*>(p.out) + ((int64_t)(qs + (row_valid ? i : 0)) * p.Hq + h * G +
+                                             r % G) * kD + cb);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          dst[c] = make_uint4(narrow2<DT>(o[8 * c] * inv, o[8 * c + 1] * inv),
-                              narrow2<DT>(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                              narrow2<DT>(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                              narrow2<DT>(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          float o[32];
+          tmem_ld32(ocol + c0, o);
+          if (row_valid) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              dst[c0 / 8 + c] = make_uint4(narrow2<DT>(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                           narrow2<DT>(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                           narrow2<DT>(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                           narrow2<DT>(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+          }
+        }
       }
     }
   }
@@ -463,7 +503,7 @@ pa_status launch_g(const PrefillParams& p, const CUtensorMap& k, const CUtensorM
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr != cudaSuccess) return PA_ERR_CUDA;
-  const dim3 grid((unsigned)p.n_qtiles, (unsigned)(p.Hkv * p.B));
+  const dim3 grid((unsigned)p.n_qpairs, (unsigned)(p.Hkv * p.B));
   if (launch_pdl(prefill_tc_kernel<DT, G>, grid, kThreads, kSmemBytes, stream, k, v, q, p) !=
       cudaSuccess)
     return PA_ERR_CUDA;
@@ -555,7 +595,7 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   p.max_blocks = max_blocks;
   p.num_blocks = num_blocks;
   p.max_q_len = max_q_len;
-  p.n_qtiles = (int)n_qtiles;
+  p.n_qpairs = (int)((n_qtiles + 1) / 2);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status_dev = status_dev;
   return dtype == PA_BFLOAT16 ? launch_dt<PA_BFLOAT16>(G, p, tk, tv, tq, stream)
