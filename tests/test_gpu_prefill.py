@@ -141,3 +141,23 @@ def test_benchmark_workloads_sampled_rows(pa, w):
     ref = scenarios.prefill_f64(pb, rows=rows)
     assert_close(widen(out)[rows], ref[rows], w.name)
     assert dev.guards_intact()
+
+
+@pytest.mark.parametrize("scale", [0.25, 1.0])
+def test_sharp_attention_every_row(pa, scale):
+    """Large softmax scales concentrate each row's weight on a few keys anywhere
+    in the sequence (logit spread 2.8 and 11): the rows where a single rounding
+    of P would break the tolerance."""
+    w = dataclasses.replace(_small(4, 16, syn.BFLOAT16, [700, 300, 129], hkv=2))
+    pb = scenarios.prefill_batch(w)
+    b = pb.batch
+    dev = DeviceBatch(b)
+    q = to_dev(pb.q, w.dtype)
+    out = torch.empty_like(q)
+    pa.pa_prefill(out, q, dev.k_pool, dev.v_pool, dev.tables, dev.lens, i32(pb.q_start), scale,
+                  max_q_len=700)
+    torch.cuda.synchronize()
+    from oracle.prefill import paged_prefill_attention
+    ref = paged_prefill_attention(pb.q, b.k_pool, b.v_pool, b.block_tables, b.seq_lens,
+                                  pb.q_start, scale, dtype=b.dtype)
+    assert_close(widen(out), ref, f"scale {scale}")
