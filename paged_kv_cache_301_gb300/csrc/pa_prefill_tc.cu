@@ -332,18 +332,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       // the tile's maximum of the visible raw scores (scale > 0 commutes with max);
       // S is read again for the exponentials (registers hold one 32-column chunk)
       float mt = -CUDART_INF_F;
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        float sv[32];
-        tmem_ld32(scol + c0, sv);
+      {
+        float sv[64];
+        tmem_ld64(scol, sv);
         if (!partial) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, sv[e]);
+          for (int e = 0; e < 64; ++e) mt = fmaxf(mt, sv[e]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, kc + c0 + e <= pos ? sv[e] : -CUDART_INF_F);
+          for (int e = 0; e < 64; ++e) mt = fmaxf(mt, kc + e <= pos ? sv[e] : -CUDART_INF_F);
         }
       }
+      // the first chunk of the second read overlaps the max exchange
+      uint32_t s0[32];
+      tmem_ld32_start(scol, s0);
       {   // over the row's two halves
         const int rb = t & 1;
         tl->red_max[k][rb][half][r] = mt;
@@ -357,21 +359,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       // t-1) and l scale by 2^(m_old - m_new).  TMEM access is warp-wide, so the
       // warp rescales when any of its rows needs it (the others by 1).
       const bool raise = m_run != -CUDART_INF_F && m_tile > m_run + kRescaleLog2;
-      if (__any_sync(0xFFFFFFFFu, raise)) {
-        const float alpha = raise ? ex2_approx(m_run - m_tile) : 1.f;
-        if (!wait_all(&tl->pv_done[k], (t - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          float o[32];
-          tmem_ld32(ocol + c0, o);
-          uint32_t ow[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ow[e] = __float_as_uint(o[e] * alpha);
-          tmem_st32(ocol + c0, ow);
-        }
-        l_run *= alpha;
-      }
+      const float alpha = raise ? ex2_approx(m_run - m_tile) : 1.f;
       if (m_run == -CUDART_INF_F || raise) m_run = m_tile;   // first visible tile, or raised
       const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
       // p = 2^(s * scale * log2 e - m), written back over the S columns as
@@ -380,7 +368,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         float sv[32];
-        tmem_ld32(scol + c0, sv);
+        if (c0 == 0) {
+          tmem_wait_ld32(s0);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sv[e] = __uint_as_float(s0[e]);
+        } else {
+          tmem_ld32(scol + c0, sv);
+        }
 #pragma unroll
         for (int g = 0; g < 32; g += 16) {
           uint32_t pw[16];
@@ -410,7 +404,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
           tmem_st16(scol + c0 + g, pw);          // over S columns already read
         }
       }
-      l_run += ls;
+      // Rows that raised their max rescale O (complete up to tile t-1, P.V(t) not
+      // yet issued) and l.  TMEM access is warp-wide: the warp rescales when any
+      // of its rows needs it (the others by 1).
+      if (__any_sync(0xFFFFFFFFu, raise)) {
+        if (!wait_all(&tl->pv_done[k], (t - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          float o[32];
+          tmem_ld32(ocol + c0, o);
+          uint32_t ow[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ow[e] = __float_as_uint(o[e] * alpha);
+          tmem_st32(ocol + c0, ow);
+        }
+      }
+      l_run = fmaf(l_run, alpha, ls);
       // keys at or past L: their V rows hold whatever the slot or an earlier tile
       // left (0 * NaN must not reach O).  The first tile whose product reads V(t)
       // zeroes them before releasing its P.
