@@ -58,17 +58,22 @@ struct Geo {
   static constexpr int N = (Hq + 15) / 16 * 16;
   static constexpr int TT = kRows / H;                   // tokens per tile
   static constexpr int kQBytes = N * 256;
-  static constexpr int kQBufs = N >= 64 ? 1 : 2;         // one buffer leaves room for a 4th stage
+  // For N = 64, Q and P' are single-buffered and the room goes to a fifth ring
+  // stage (measured on GB300: long-context decode 90% -> 95% of the HBM peak).
+  // For N = 32 the same trade (six stages) measured slower (82% -> 79.5%): the
+  // softmax then waits for the previous P'.V before writing P'.
+  static constexpr int kQBufs = N >= 64 ? 1 : 2;
+  static constexpr int kPBufs = N >= 64 ? 1 : 2;
   static constexpr int kPHalf = N * 256;
   static constexpr int kPBytes = 2 * kPHalf;
   // as many 32 KB ring stages as the shared memory left over allows
-  static constexpr int kFree = kSmemBudget - kTailReserve - kQBufs * kQBytes - 2 * kPBytes;
+  static constexpr int kFree = kSmemBudget - kTailReserve - kQBufs * kQBytes - kPBufs * kPBytes;
   static constexpr int kStages = kFree / kStage > kMaxStages ? kMaxStages : kFree / kStage;
   static constexpr uint32_t kTmemCols = 4 * N < 64 ? 64 : 4 * N;
   static constexpr int kRingOff = 0;
   static constexpr int kQOff = kStages * kStage;
   static constexpr int kPOff = kQOff + kQBufs * kQBytes;
-  static constexpr int kTailOff = kPOff + 2 * kPBytes;
+  static constexpr int kTailOff = kPOff + kPBufs * kPBytes;
 };
 
 struct SegInfo {
@@ -173,7 +178,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
   if (warp >= 2) {
     // P' is block diagonal: entries outside a row's query group stay zero forever
     uint4* pz = reinterpret_cast<uint4*>(smem + Gm::kPOff);
-    for (int i = threadIdx.x - 64; i < 2 * Gm::kPBytes / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x - 64; i < Gm::kPBufs * Gm::kPBytes / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
     fence_async_smem();
   }
   allow_next_grid();
@@ -402,11 +407,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     auto issue_pv = [&](int t, int vs, int vph) -> bool {
       const int slot = t & 1, ph = (t >> 1) & 1;
       if (!mbar_wait(&tl->full[vs], vph, abort_flag, kWaitNs)) return false;
-      if (!mbar_wait(&tl->p_full[slot], ph, abort_flag, kWaitNs)) return false;
+      const int ps = t % Gm::kPBufs, pph = (t / Gm::kPBufs) & 1;
+      if (!mbar_wait(&tl->p_full[ps], pph, abort_flag, kWaitNs)) return false;
       if (!mbar_wait(&tl->o_empty[slot], ph ^ 1, abort_flag, kWaitNs)) return false;
       tc_fence_after();
       const uint32_t vaddr = ring_addr + vs * kStage;
-      const uint32_t paddr = p_addr + slot * Gm::kPBytes;
+      const uint32_t paddr = p_addr + ps * Gm::kPBytes;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -419,7 +425,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       mma_commit(&tl->empty[vs]);
       mma_commit(&tl->o_full[slot]);
-      mma_commit(&tl->p_empty[slot]);
+      mma_commit(&tl->p_empty[ps]);
       return true;
     };
     for (;;) {
@@ -590,8 +596,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
           for (int g = 0; g < G; ++g) tl->alpha[rb][h * G + g] = alpha[g];
         }
         // P' entries of this row: (head h*G+g, column r)
-        if (!wait_all(&tl->p_empty[slot], ph ^ 1)) { ok = false; break; }
-        uint8_t* pbuf = smem + Gm::kPOff + slot * Gm::kPBytes + (r >> 6) * (N * 128);
+        const int ps = t % Gm::kPBufs, pph = (t / Gm::kPBufs) & 1;
+        if (!wait_all(&tl->p_empty[ps], pph ^ 1)) { ok = false; break; }
+        uint8_t* pbuf = smem + Gm::kPOff + ps * Gm::kPBytes + (r >> 6) * (N * 128);
         const int chunk = (r & 63) >> 3;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -620,7 +627,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->p_full[slot]);
+        if (lane == 0) mbar_arrive(&tl->p_full[ps]);
         if (j > 0 && !accumulate(t - 1, round - 1)) { ok = false; break; }
         ++round;
       }
