@@ -164,13 +164,17 @@ def gpu_uuid(torch, dev) -> str | None:
 # native arm
 # ----------------------------------------------------------------------------
 
+# the grouped decode kernel, its launch code and the headers it includes
+DECODE_SOURCES = ("pa_api.cu", "pa_decode_tcg.cu", "pa_common.cuh", "pa_internal.h",
+                  "pa_sm100.cuh")
+
+
 def kernel_sources_sha() -> str:
     csrc = os.path.join(ROOT, "paged_kv_cache_301_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in DECODE_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
