@@ -265,8 +265,7 @@ pa_status pa_append_tokens(void* k_pool, void* v_pool, const void* key, const vo
  * seq_lens[b] > max_blocks * block_size, or rows outside [0, total_q) is skipped
  * (rows untouched; reported in checked mode); out-of-range block ids read zeros
  * (reported in checked mode).
- * No workspace.  Kernel: tcgen05 tensor cores, TMA, one CTA per (sequence, KV
- * head, tile of 128 / G query tokens x G heads).
+ * No workspace.
  */
 pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                      const int32_t* block_tables, const int32_t* seq_lens,

@@ -248,3 +248,26 @@ def test_bad_arguments_raise(pa):
     with pytest.raises(pa.PagedAttnError):
         pa.pa_decode(torch.empty_like(dev.q), dev.q, dev.k_pool, dev.v_pool, dev.tables,
                      dev.lens, 0.125, max_seq_len=64, workspace=ws)
+
+
+def test_one_workspace_serves_a_sequence_of_batches(pa):
+    """One workspace reused by consecutive decodes of different batches (many
+    short sequences, then few long ones): nothing a call leaves in it affects the
+    next, and a repeated batch gives identical bits."""
+    w1 = dataclasses.replace(syn.LLAMA3_8B, num_seqs=64, lo=100, hi=1500)
+    w2 = dataclasses.replace(syn.LLAMA3_8B, num_seqs=40, lo=500, hi=3000, seed=9)
+    w3 = dataclasses.replace(syn.LLAMA3_8B, num_seqs=4, lo=3000, hi=9000, seed=10)
+    batches = [scenarios.fixed_batch(w, fill_all=True) for w in (w1, w2, w3)]
+    ws = pa.alloc_workspace(64, 32, 128, 9000)
+    outs = []
+    for batch in batches + batches[:1]:
+        dev = DeviceBatch(batch)
+        out = torch.empty_like(dev.q)
+        pa.pa_decode(out, dev.q, dev.k_pool, dev.v_pool, dev.tables, dev.lens, batch.scale,
+                     max_seq_len=int(batch.seq_lens.max()), workspace=ws)
+        torch.cuda.synchronize()
+        rows = list(range(0, len(batch.seq_lens), 7))
+        assert_close(widen(out)[rows], scenarios.decode_f64(batch, sequences=rows)[rows],
+                     f"batch of {len(batch.seq_lens)}")
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[3].view(torch.int16))
