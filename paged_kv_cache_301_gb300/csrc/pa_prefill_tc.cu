@@ -232,28 +232,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const uint32_t ring = smem_addr(smem + kRingOff);
     const uint32_t qaddr = smem_addr(smem + kQOff);
     bool ok = true, committed = false;
+    // One thread issues every MMA, one per 64 tensor cycles at full rate, so the
+    // shared-memory descriptors are built once per operand and stepped by
+    // compile-time offsets (the start-address field holds address / 16).
+    const uint64_t qdesc_a = smem_desc_sw128(qaddr, 16, 1024);
+    const uint64_t qdesc_b = smem_desc_sw128(qaddr + kTile, 16, 1024);
     // S_k = Q_k . K(t)^T into S/P buffer k
     auto issue_s = [&](int k, int t) {
-      const uint32_t kaddr = ring + ((2 * t) % kStages) * kTile;
+      const uint64_t kdesc = smem_desc_sw128(ring + ((2 * t) % kStages) * kTile, 16, 1024);
+      const uint64_t q0d = k ? qdesc_b : qdesc_a;
+      const uint32_t d = tmem + k * kKeys;
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
-        mma_f16(tmem + k * kKeys, smem_desc_sw128(qaddr + k * kTile + off, 16, 1024),
-                smem_desc_sw128(kaddr + off, 16, 1024), idesc_s, kk > 0);
+        const uint64_t off = (uint64_t)(((kk >> 2) * kSlab + (kk & 3) * 32) >> 4);
+        mma_f16(d, q0d + off, kdesc + off, idesc_s, kk > 0);
       }
       mma_commit(&tl->s_full[k]);
     };
     // O_k += (P_hi + P_lo) . V(t).  P sits in S/P buffer k: 16-key group g occupies
     // columns 16g .. 16g+7 (hi) and 16g+8 .. 16g+15 (lo).
     auto issue_pv = [&](int k, int t) {
-      const uint32_t vaddr = ring + ((2 * t + 1) % kStages) * kTile;
+      const uint64_t vdesc = smem_desc_sw128(ring + ((2 * t + 1) % kStages) * kTile, kSlab, 1024);
+      const uint32_t d = tmem + 256 + k * kD, pcol = tmem + k * kKeys;
 #pragma unroll
       for (int kk = 0; kk < kKeys / 16; ++kk) {
-        const uint64_t bd = smem_desc_sw128(vaddr + kk * 16 * 128, kSlab, 1024);
+        const uint64_t bd = vdesc + (uint64_t)((kk * 16 * 128) >> 4);
 #pragma unroll
         for (int term = 0; term < 2; ++term)
-          mma_f16_ts(tmem + 256 + k * kD, tmem + k * kKeys + kk * 16 + term * 8, bd, idesc_o,
-                     (t | kk | term) != 0);
+          mma_f16_ts(d, pcol + kk * 16 + term * 8, bd, idesc_o, (t | kk | term) != 0);
       }
       mma_commit(&tl->pv_done[k]);
     };
