@@ -411,16 +411,19 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (!mbar_wait(&tl->p_full[ps], pph, abort_flag, kWaitNs)) return false;
       if (!mbar_wait(&tl->o_empty[slot], ph ^ 1, abort_flag, kWaitNs)) return false;
       tc_fence_after();
-      const uint32_t vaddr = ring_addr + vs * kStage;
-      const uint32_t paddr = p_addr + ps * Gm::kPBytes;
+      // descriptors built once and stepped by compile-time offsets (address / 16):
+      // one thread issues every MMA
+      const uint64_t vdesc = smem_desc_sw128(ring_addr + vs * kStage, kSlab, 1024);
+      const uint64_t pdesc = smem_desc_sw128(p_addr + ps * Gm::kPBytes, 16, 1024);
+      const uint32_t d = tmem + 2 * N + slot * N;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
 #pragma unroll
         for (int kk = 0; kk < kRows / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(vaddr + kk * 16 * 128, kSlab, 1024);
-          const uint64_t bd = smem_desc_sw128(
-              paddr + half * Gm::kPHalf + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024);
-          mma_f16(tmem + 2 * N + slot * N, a, bd, idesc_o, (half | kk) != 0);
+          const uint64_t a = vdesc + (uint64_t)((kk * 16 * 128) >> 4);
+          const uint64_t bd =
+              pdesc + (uint64_t)((half * Gm::kPHalf + (kk >> 2) * (N * 128) + (kk & 3) * 32) >> 4);
+          mma_f16(d, a, bd, idesc_o, (half | kk) != 0);
         }
       }
       mma_commit(&tl->empty[vs]);
@@ -460,14 +463,14 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
                mbar_wait(&tl->s_empty[slot], ph ^ 1, abort_flag, kWaitNs);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t kaddr = ring_addr + ks * kStage;
-          const uint32_t qaddr = q_addr + qb * Gm::kQBytes;
+          const uint64_t kdesc = smem_desc_sw128(ring_addr + ks * kStage, 16, 1024);
+          const uint64_t qdesc = smem_desc_sw128(q_addr + qb * Gm::kQBytes, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
             const uint32_t qoff = (kk >> 2) * (N * 128) + (kk & 3) * 32;
-            mma_f16(tmem + slot * N, smem_desc_sw128(kaddr + off, 16, 1024),
-                    smem_desc_sw128(qaddr + qoff, 16, 1024), idesc_s, kk > 0);
+            mma_f16(tmem + slot * N, kdesc + (uint64_t)(off >> 4), qdesc + (uint64_t)(qoff >> 4),
+                    idesc_s, kk > 0);
           }
           mma_commit(&tl->empty[ks]);
           mma_commit(&tl->s_full[slot]);
