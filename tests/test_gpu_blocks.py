@@ -148,3 +148,19 @@ def test_sequences_swapped_to_cpu_and_back_decode_identically(pa, bs):
                        max_seq_len=int(batch.seq_lens.max()))
     assert torch.equal(after.view(torch.int16), before.view(torch.int16))
     assert_close(widen(after), scenarios.decode_f64(rt.after), f"swap bs={bs}")
+
+
+def test_swap_bad_ids_reported_and_skipped(pa):
+    g = np.random.default_rng(12)
+    gbits = _layer_pools(g, 1, 10, (16, 8, 128), syn.BFLOAT16)
+    cbits = _layer_pools(g, 1, 4, (16, 8, 128), syn.BFLOAT16)
+    gpu = [to_dev(b, syn.BFLOAT16) for b in gbits]
+    cpu = [_pinned_like(b, syn.BFLOAT16) for b in cbits]
+    pairs = np.array([[9, 0], [3, 4], [10, 1], [2, 3]], dtype=np.int32)   # dst 4 / src 10 invalid
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_swap_blocks(cpu, gpu, i32(pairs), status=status)
+    swap_blocks(cbits, gbits, pairs[[0, 3]])
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
+    for c, b in zip(cpu, cbits):
+        assert np.array_equal(_cpu_bits(c), b)

@@ -182,3 +182,31 @@ def test_ragged_continuous_batching_steps(pa, bs):
         assert_close(got[rows], ref[rows], f"bs={bs} step {i}")
     torch.cuda.synchronize()
     _pools_equal(dev, final.k_pool, final.v_pool)
+
+
+def test_append_tokens_reports_bad_lengths_and_ids(pa):
+    """Checked mode: a length past its table and a block id outside the pool are
+    reported and skipped; every other sequence is written."""
+    initial, steps, final = scenarios.ragged_steps(syn.RAGGED, 16, 1, num_seqs=12)
+    st = steps[0]
+    dev = DeviceBatch(initial)
+    dt = syn.RAGGED.dtype
+    lens = st.seq_lens.copy()
+    tables = st.block_tables.copy()
+    lens[2] = tables.shape[1] * 16 + 5                     # longer than its table
+    row = (lens[7] - 1) // 16
+    tables[7, row] = initial.num_blocks + 3                # the newest token's block: outside
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.empty(len(lens), dtype=torch.int32, device="cuda")
+    pa.pa_append_tokens(dev.k_pool, dev.v_pool, to_dev(st.key, dt), to_dev(st.value, dt),
+                        i32(tables), i32(lens), slot_mapping=slots, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
+    got = slots.cpu().numpy()
+    assert got[2] == -1 and got[7] == -1
+    want = st.slot_mapping.copy()
+    want[[2, 7]] = -1
+    assert np.array_equal(got, want)
+    k_ref, v_ref = initial.k_pool.copy(), initial.v_pool.copy()
+    reshape_and_cache(k_ref, v_ref, st.key, st.value, want)
+    _pools_equal(dev, k_ref, v_ref)

@@ -161,3 +161,22 @@ def test_sharp_attention_every_row(pa, scale):
     ref = paged_prefill_attention(pb.q, b.k_pool, b.v_pool, b.block_tables, b.seq_lens,
                                   pb.q_start, scale, dtype=b.dtype)
     assert_close(widen(out), ref, f"scale {scale}")
+
+
+def test_bad_block_id_reported_and_read_as_zeros(pa):
+    """Checked mode: a table entry outside the pool is reported; the kernel reads
+    zeros there (never outside the pool), so the other sequences are unaffected."""
+    w = _small(4, 16, syn.BFLOAT16, [200, 90], hkv=2)
+    pb = scenarios.prefill_batch(w)
+    b = pb.batch
+    good, dev = _run(pa, pb)
+    tables = b.block_tables.copy()
+    tables[0, 3] = b.num_blocks + 100
+    bad = dataclasses.replace(pb, batch=dataclasses.replace(b, block_tables=tables))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev.tables = i32(tables)
+    out, _ = _run(pa, bad, dev=dev, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
+    assert torch.equal(out[200:].view(torch.int16), good[200:].view(torch.int16))
+    assert torch.isfinite(out[:200].float()).all()
