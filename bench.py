@@ -582,6 +582,7 @@ def run_prefill(args):
     def dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(dt)
 
+    pa.set_prefill_path("simt" if args.kernel == "simt" else "auto")
     kp, vp, q = dev(b.k_pool), dev(b.v_pool), dev(pb.q)
     tables = torch.from_numpy(b.block_tables).cuda()
     lens = torch.from_numpy(b.seq_lens).cuda()
@@ -647,7 +648,8 @@ def run_prefill(args):
                    "block_size": w.block_size, "total_tokens": int(b.seq_lens.sum()),
                    "query_tokens": total_q, "causal_pairs_per_head": pairs},
         "tokens_per_s": round(total_q / (ms * 1e-3), 1),
-        "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor",
+        "roofline": {"kernel": "prefill_simt_kernel" if args.kernel == "simt" else "prefill_tc_kernel",
+                     "bound": "tensor",
                      "achieved": round(tflops, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                      "algorithmic_flops": flops, "avg_launch_ms": round(ms, 5)},

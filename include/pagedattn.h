@@ -259,9 +259,10 @@ pa_status pa_append_tokens(void* k_pool, void* v_pool, const void* key, const vo
  * For query head hq of that row, with KV head h = hq / (num_q_heads /
  * num_kv_heads):  out = softmax_t(scale * q . K[slot_t, h]) . V[slot_t, h] over
  * t = 0 .. position, slot_t as in pa_decode.  fp32 accumulation, output rounded
- * to the storage type.  Supported: head_dim 128, num_q_heads / num_kv_heads in
- * {1, 2, 4, 8, 16}, block_size in {8, 16, 32, 64}; other shapes return
- * PA_ERR_UNSUPPORTED.  A sequence with n_b > seq_lens[b], n_b > max_q_len,
+ * to the storage type.  Supported: head_dim 64 or 128, any num_q_heads /
+ * num_kv_heads, block_size in {8, 16, 32, 64}, fp16 / bf16.  head_dim 128 with
+ * query groups of 1, 2, 4, 8 or 16 runs on the tensor cores (tcgen05, TMA); every
+ * other shape on a CUDA-core kernel.  A sequence with n_b > seq_lens[b], n_b > max_q_len,
  * seq_lens[b] > max_blocks * block_size, or rows outside [0, total_q) is skipped
  * (rows untouched; reported in checked mode); out-of-range block ids read zeros
  * (reported in checked mode).
@@ -273,6 +274,13 @@ pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v
                      int num_kv_heads, int head_dim, int block_size, int max_blocks,
                      int num_blocks, int max_q_len, float scale, int dtype,
                      int32_t* status_dev, cudaStream_t stream);
+
+/* Kernel choice for pa_prefill (process-wide; for tests and measurements):
+ * AUTO picks the tensor-core kernel where it serves the shape. */
+typedef enum pa_prefill_path {
+  PA_PREFILL_AUTO = 0, PA_PREFILL_SIMT = 1, PA_PREFILL_TC = 2
+} pa_prefill_path;
+pa_status pa_set_prefill_path(int path);
 
 /*
  * Copy-on-write across a whole model in one launch ("10 — Paged Attention"

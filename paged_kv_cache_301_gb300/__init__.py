@@ -213,6 +213,14 @@ def pa_decode_slots(slot_mapping: torch.Tensor, block_tables: torch.Tensor,
     return slot_mapping
 
 
+PREFILL_PATHS = {"auto": 0, "simt": 1, "tc": 2}
+
+
+def set_prefill_path(path: str) -> None:
+    """Choose pa_prefill's kernel: "auto", "simt" (CUDA cores) or "tc"."""
+    _check(lib().pa_set_prefill_path(PREFILL_PATHS[path]), "pa_set_prefill_path")
+
+
 def pa_prefill(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                block_tables: torch.Tensor, seq_lens: torch.Tensor, q_start: torch.Tensor,
                scale: float, max_q_len: Optional[int] = None,
@@ -393,7 +401,7 @@ class BlockManager:
 __all__ = [
     "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_workspace_bytes",
     "pa_decode_noalloc", "set_decode_path",
-    "alloc_workspace", "pa_reshape_and_cache", "pa_append_tokens", "pa_prefill",
+    "alloc_workspace", "pa_reshape_and_cache", "pa_append_tokens", "pa_prefill", "set_prefill_path",
     "pa_copy_blocks_multi", "pa_swap_blocks", "pa_copy_blocks", "pa_decode_slots",
     "BlockManager", "lib", "simulate_allocator",
 ]

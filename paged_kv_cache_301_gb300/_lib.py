@@ -34,6 +34,7 @@ SIGNATURES = {
     "pa_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_void_p, c_void_p]),
     "pa_set_decode_path": (c_int, [c_int]),
+    "pa_set_prefill_path": (c_int, [c_int]),
     "pa_prefill": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                            c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                            ctypes.c_float, c_int, c_void_p, c_void_p]),

@@ -51,4 +51,21 @@ SkLayout sk_layout(int B, int Hq);
 bool tcg_supported(const DecodeParams& p);
 pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t stream);
 
+// Prefill (causal multi-query attention over the pool), resolved on the host.
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* tables;
+  const int32_t* seq_lens;
+  const int32_t* q_start;
+  int B, total_q, Hq, Hkv, D, bs, max_blocks, num_blocks, max_q_len;
+  float scale_log2;
+  int dtype;
+  int32_t* status_dev;
+};
+// CUDA-core kernel for every supported shape (head_dim 64 or 128, any group).
+pa_status launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
+
 }  // namespace pa

@@ -38,6 +38,7 @@
 #include <mutex>
 
 #include "pa_common.cuh"
+#include "pa_internal.h"
 #include "pa_sm100.cuh"
 
 namespace pa {
@@ -546,6 +547,14 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
 using namespace pa;
 
+static int g_prefill_path = PA_PREFILL_AUTO;
+
+extern "C" pa_status pa_set_prefill_path(int path) {
+  if (path < PA_PREFILL_AUTO || path > PA_PREFILL_TC) return PA_ERR_INVALID_ARG;
+  g_prefill_path = path;
+  return PA_OK;
+}
+
 extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v_pool,
                                 const int32_t* block_tables, const int32_t* seq_lens,
                                 const int32_t* q_start, int num_seqs, int total_q,
@@ -557,10 +566,13 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
       !(scale > 0.f) || !(scale < 3.0e38f))
     return PA_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
-  if (head_dim != kD || (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) ||
+  if ((head_dim != 64 && head_dim != 128) ||
       (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64) ||
       (dtype != PA_FLOAT16 && dtype != PA_BFLOAT16))
     return PA_ERR_UNSUPPORTED;
+  const int path = g_prefill_path;
+  const bool tc_shape = head_dim == kD && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
+  if (path == PA_PREFILL_TC && !tc_shape) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PA_OK;
   if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !q_start)
     return PA_ERR_INVALID_ARG;
@@ -569,11 +581,33 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   if ((int64_t)num_blocks * block_size >= (1ll << 31) ||
       (int64_t)total_q * num_q_heads >= (1ll << 31))
     return PA_ERR_INVALID_ARG;
+  EncodeTiledFn enc = encode_fn();
+  if (!tc_shape || path == PA_PREFILL_SIMT || !enc) {
+    PrefillArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.q_start = q_start;
+    a.B = num_seqs;
+    a.total_q = total_q;
+    a.Hq = num_q_heads;
+    a.Hkv = num_kv_heads;
+    a.D = head_dim;
+    a.bs = block_size;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.max_q_len = max_q_len;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.dtype = dtype;
+    a.status_dev = status_dev;
+    return launch_prefill_simt(a, stream);
+  }
   const int TQ = kRows / G;
   const int64_t n_qtiles = ((int64_t)max_q_len + TQ - 1) / TQ;
   if ((int64_t)num_seqs * num_kv_heads > 65535) return PA_ERR_INVALID_ARG;   // grid y
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return PA_ERR_UNSUPPORTED;
 
   const CUtensorMapDataType dt =
       dtype == PA_BFLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;

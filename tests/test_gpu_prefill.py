@@ -15,9 +15,15 @@ from tests.gpu_helpers import DeviceBatch, assert_close, i32, lib, to_dev, widen
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def pa():
-    return lib()
+@pytest.fixture(scope="module", params=["auto", "simt"])
+def pa(request):
+    """Every test runs on the default choice (the tensor-core kernel where it
+    serves the shape) and on the CUDA-core kernel."""
+    m = lib()
+    m.set_prefill_path(request.param)
+    m.prefill_path = request.param
+    yield m
+    m.set_prefill_path("auto")
 
 
 def _run(pa, pb, dev=None, status=None, max_q_len=None):
@@ -114,17 +120,35 @@ def test_deterministic_and_bad_input_reported(pa):
     assert torch.equal(out[:500].view(torch.int16), a[:500].view(torch.int16))
 
 
-def test_unsupported_shapes_refused(pa):
-    w = _small(4, 16, syn.BFLOAT16, [10], hkv=2)
+@pytest.mark.parametrize("dtype", [syn.FLOAT16, syn.BFLOAT16])
+@pytest.mark.parametrize("head_dim,hq,hkv", [(64, 4, 4), (64, 12, 4), (128, 24, 4), (128, 6, 2)])
+def test_other_shapes_every_row(pa, dtype, head_dim, hq, hkv):
+    """head_dim 64 and query groups outside 1/2/4/8/16 (the CUDA-core kernel)."""
+    w = dataclasses.replace(syn.PREFILL, name="pf_other", num_seqs=4, length_kind="fixed",
+                            lens=(1, 70, 200, 33), num_q_heads=hq, num_kv_heads=hkv,
+                            head_dim=head_dim, block_size=16, dtype=dtype)
+    pb = scenarios.prefill_batch(w, q_counts=(1, 70, 50, 10))
+    out, dev = _run(pa, pb)
+    torch.cuda.synchronize()
+    assert_close(widen(out), scenarios.prefill_f64(pb), f"D={head_dim} Hq={hq} Hkv={hkv}")
+    assert dev.guards_intact()
+
+
+def test_forcing_tensor_cores_on_other_shapes_is_refused(pa):
+    w = dataclasses.replace(syn.PREFILL, name="pf_d64", num_seqs=1, length_kind="fixed",
+                            lens=(10,), num_q_heads=4, num_kv_heads=2, head_dim=64)
     pb = scenarios.prefill_batch(w)
     dev = DeviceBatch(pb.batch)
     q = to_dev(pb.q, w.dtype)
     out = torch.empty_like(q)
-    with pytest.raises(pa.PagedAttnError) as ei:
-        pa.pa_prefill(out[:, :, :64].contiguous(), q[:, :, :64].contiguous(), dev.k_pool[..., :64].contiguous(),
-                      dev.v_pool[..., :64].contiguous(), dev.tables, dev.lens, i32(pb.q_start),
-                      w.scale, max_q_len=10)
-    assert ei.value.status == 2
+    pa.set_prefill_path("tc")
+    try:
+        with pytest.raises(pa.PagedAttnError) as ei:
+            pa.pa_prefill(out, q, dev.k_pool, dev.v_pool, dev.tables, dev.lens, i32(pb.q_start),
+                          w.scale, max_q_len=10)
+        assert ei.value.status == 2
+    finally:
+        pa.set_prefill_path(pa.prefill_path)
 
 
 @pytest.mark.parametrize("w", [syn.PREFILL, syn.CHUNKED_PREFILL], ids=lambda w: w.name)
