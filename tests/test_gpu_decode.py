@@ -271,3 +271,13 @@ def test_one_workspace_serves_a_sequence_of_batches(pa):
                      f"batch of {len(batch.seq_lens)}")
         outs.append(out)
     assert torch.equal(outs[0].view(torch.int16), outs[3].view(torch.int16))
+
+
+def test_more_sequences_than_the_grouped_kernel_serves(pa):
+    """1,100 short sequences: past the grouped kernel's 1,023-sequence limit, the
+    call takes another kernel and stays exact within the tolerance."""
+    w = _small("llama3_8b", num_seqs=1100, length_kind="uniform", lo=1, hi=300, seed=77)
+    batch = scenarios.fixed_batch(w, fill_all=True)
+    got = widen(DeviceBatch(batch).decode(pa))
+    rows = list(range(0, 1100, 37)) + [1099]
+    assert_close(got[rows], scenarios.decode_f64(batch, sequences=rows)[rows], "B=1100")

@@ -204,3 +204,17 @@ def test_bad_block_id_reported_and_read_as_zeros(pa):
     assert int(status.item()) == 5
     assert torch.equal(out[200:].view(torch.int16), good[200:].view(torch.int16))
     assert torch.isfinite(out[:200].float()).all()
+
+
+def test_many_sequences(pa):
+    """300 sequences with 1-40 query tokens each over contexts of up to 600."""
+    g = np.random.default_rng(5)
+    lens = tuple(int(x) for x in g.integers(1, 600, size=300))
+    w = dataclasses.replace(syn.PREFILL, name="pf_many", num_seqs=300, length_kind="fixed",
+                            lens=lens, num_q_heads=32, num_kv_heads=8)
+    q_counts = tuple(int(min(L, c)) for L, c in zip(lens, g.integers(1, 41, size=300)))
+    pb = scenarios.prefill_batch(w, q_counts=q_counts)
+    out, _ = _run(pa, pb)
+    torch.cuda.synchronize()
+    rows = sorted(set(int(x) for x in g.integers(0, int(pb.q_start[-1]), size=60)))
+    assert_close(widen(out)[rows], scenarios.prefill_f64(pb, rows=rows)[rows], "B=300")
