@@ -281,17 +281,29 @@ class NativeStep:
             self.launches_per_step = 1 + 1 + (1 if P > 1 else 0)
         if self.pairs is not None:      # copy-on-write block copies
             self.launches_per_step += 1
-        # pinned host copies for the end-to-end measurement
-        self.h_q = self.q.cpu().pin_memory()
-        self.h_key = self.key.cpu().pin_memory()
-        self.h_value = self.value.cpu().pin_memory()
-        self.h_tables = self.tables.cpu().pin_memory()
-        self.h_lens = self.seq_lens.cpu().pin_memory()
+        # End-to-end measurement: every step's inputs (q, the new tokens' K/V,
+        # tables, lengths, copy-on-write pairs) live packed in one pinned host
+        # buffer mirrored by one device buffer, whose views the step uses, so a
+        # step moves them with one host-to-device copy; the output comes back
+        # with one device-to-host copy.
+        parts = [("q", self.q), ("key", self.key), ("value", self.value),
+                 ("tables", self.tables), ("seq_lens", self.seq_lens)]
+        if self.pairs is not None:
+            parts.append(("pairs", self.pairs))
+        offs, total = [], 0
+        for _, t in parts:
+            offs.append(total)
+            total += -(-t.numel() * t.element_size() // 256) * 256
+        self.d_in = torch.empty(total, dtype=torch.uint8, device=dev)
+        self.h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+        for (name, t), off in zip(parts, offs):
+            n = t.numel() * t.element_size()
+            dview = self.d_in[off:off + n].view(t.dtype).view(t.shape)
+            dview.copy_(t)
+            self.h_in[off:off + n].view(t.dtype).view(t.shape).copy_(t.cpu())
+            setattr(self, name, dview)
         self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self.h_pairs = self.pairs.cpu().pin_memory() if self.pairs is not None else None
-        self.h2d_bytes = sum(t.numel() * t.element_size() for t in
-                             (self.h_q, self.h_key, self.h_value, self.h_tables, self.h_lens)
-                             + ((self.h_pairs,) if self.h_pairs is not None else ()))
+        self.h2d_bytes = sum(t.numel() * t.element_size() for _, t in parts)
         self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
 
     def write_step(self):
@@ -311,14 +323,8 @@ class NativeStep:
         self.decode()
 
     def run_e2e(self):
-        # step inputs from pinned host memory, result back to pinned host memory
-        self.q.copy_(self.h_q, non_blocking=True)
-        self.key.copy_(self.h_key, non_blocking=True)
-        self.value.copy_(self.h_value, non_blocking=True)
-        self.tables.copy_(self.h_tables, non_blocking=True)
-        self.seq_lens.copy_(self.h_lens, non_blocking=True)
-        if self.h_pairs is not None:
-            self.pairs.copy_(self.h_pairs, non_blocking=True)
+        # the step's inputs from pinned host memory (one copy), the result back
+        self.d_in.copy_(self.h_in, non_blocking=True)
         self.run()
         self.h_out.copy_(self.out, non_blocking=True)
 
