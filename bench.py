@@ -194,8 +194,8 @@ def recorded_traffic(workload_name: str, kernel: str):
 
 def decode_kernel_for(w, kernel: str) -> str:
     """Which decode kernel runs (mirrors the library's selection)."""
-    grouped = (w.head_dim == 128 and w.num_kv_heads in (4, 8) and w.group in (1, 2, 4, 8)
-               and w.num_seqs <= 1023)
+    grouped = (w.head_dim == 128 and w.num_kv_heads in (1, 2, 4, 8, 16, 32)
+               and w.group in (1, 2, 4, 8) and w.num_q_heads <= 64 and w.num_seqs <= 1023)
     if kernel in ("auto", "tc"):
         if grouped:
             return "tcg"
@@ -891,7 +891,7 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="llama3_8b",
                     choices=["llama3_8b", "long_context", "shared_prefix", "ragged", "tiny",
-                             "prefill", "chunked_prefill"])
+                             "mha_7b", "prefill", "chunked_prefill"])
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_head"], default="auto")

@@ -805,14 +805,40 @@ pa_status launch_t(const SkParams& sp, const CUtensorMap& k, const CUtensorMap& 
   return PA_OK;
 }
 
+// Query heads of a sequence: at most kMaxHq (thread d of the softmax warps holds
+// one accumulator per query head).
+constexpr int kMaxHq = 64;
+
+template <int DT, int H, int G>
+pa_status launch_hg(const SkParams& sp, const CUtensorMap& k, const CUtensorMap& v,
+                    const CUtensorMap& q, int grid, cudaStream_t stream) {
+  if constexpr (H * G <= kMaxHq) return launch_t<DT, H, G>(sp, k, v, q, grid, stream);
+  else return PA_ERR_UNSUPPORTED;
+}
+
 template <int DT, int H>
 pa_status launch_h(int G, const SkParams& sp, const CUtensorMap& k, const CUtensorMap& v,
                    const CUtensorMap& q, int grid, cudaStream_t stream) {
   switch (G) {
-    case 1: return launch_t<DT, H, 1>(sp, k, v, q, grid, stream);
-    case 2: return launch_t<DT, H, 2>(sp, k, v, q, grid, stream);
-    case 4: return launch_t<DT, H, 4>(sp, k, v, q, grid, stream);
-    case 8: return launch_t<DT, H, 8>(sp, k, v, q, grid, stream);
+    case 1: return launch_hg<DT, H, 1>(sp, k, v, q, grid, stream);
+    case 2: return launch_hg<DT, H, 2>(sp, k, v, q, grid, stream);
+    case 4: return launch_hg<DT, H, 4>(sp, k, v, q, grid, stream);
+    case 8: return launch_hg<DT, H, 8>(sp, k, v, q, grid, stream);
+    default: return PA_ERR_UNSUPPORTED;
+  }
+}
+
+// KV heads per block: a tile is 128 rows = 128 / H tokens x H heads
+template <int DT>
+pa_status launch_dt(int H, int G, const SkParams& sp, const CUtensorMap& k, const CUtensorMap& v,
+                    const CUtensorMap& q, int grid, cudaStream_t stream) {
+  switch (H) {
+    case 1: return launch_h<DT, 1>(G, sp, k, v, q, grid, stream);
+    case 2: return launch_h<DT, 2>(G, sp, k, v, q, grid, stream);
+    case 4: return launch_h<DT, 4>(G, sp, k, v, q, grid, stream);
+    case 8: return launch_h<DT, 8>(G, sp, k, v, q, grid, stream);
+    case 16: return launch_h<DT, 16>(G, sp, k, v, q, grid, stream);
+    case 32: return launch_h<DT, 32>(G, sp, k, v, q, grid, stream);
     default: return PA_ERR_UNSUPPORTED;
   }
 }
@@ -822,9 +848,11 @@ pa_status launch_h(int G, const SkParams& sp, const CUtensorMap& k, const CUtens
 bool tcg_supported(const DecodeParams& p) {
   const int G = p.Hq / p.Hkv;
   if (p.D != kD) return false;
-  if (p.Hkv != 4 && p.Hkv != 8) return false;
+  if (p.Hkv != 1 && p.Hkv != 2 && p.Hkv != 4 && p.Hkv != 8 && p.Hkv != 16 && p.Hkv != 32)
+    return false;
   if (p.B > kMaxSeqs) return false;
   if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+  if (p.Hq > kMaxHq) return false;
   if ((long long)p.num_blocks * p.bs >= (1ll << 31)) return false;
   if ((long long)p.B * p.Hq >= (1ll << 31)) return false;
   return encode_fn() != nullptr;
@@ -884,13 +912,9 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
   sp.part_l = reinterpret_cast<float*>(ws + l.l_off);
   sp.part_acc = reinterpret_cast<float*>(ws + l.acc_off);
 
-  pa_status st;
-  if (p.dtype == PA_BFLOAT16)
-    st = H == 4 ? launch_h<PA_BFLOAT16, 4>(G, sp, tk, tv, tq, grid, stream)
-                : launch_h<PA_BFLOAT16, 8>(G, sp, tk, tv, tq, grid, stream);
-  else
-    st = H == 4 ? launch_h<PA_FLOAT16, 4>(G, sp, tk, tv, tq, grid, stream)
-                : launch_h<PA_FLOAT16, 8>(G, sp, tk, tv, tq, grid, stream);
+  const pa_status st = p.dtype == PA_BFLOAT16
+                           ? launch_dt<PA_BFLOAT16>(H, G, sp, tk, tv, tq, grid, stream)
+                           : launch_dt<PA_FLOAT16>(H, G, sp, tk, tv, tq, grid, stream);
   if (st != PA_OK) return st;
   const long long rows = (long long)p.B * p.Hq;
   if (rows == 0) return PA_OK;

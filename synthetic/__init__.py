@@ -109,6 +109,11 @@ RAGGED = Workload(
 
 RAGGED_BLOCK_SIZES = (8, 16, 32, 64)
 
+# Plain multi-head attention (Llama-2-7B-shaped: 32 query heads, 32 KV heads).
+MHA_7B = Workload(
+    name="mha_7b", num_seqs=64, num_q_heads=32, num_kv_heads=32, head_dim=128,
+    block_size=16, dtype=BFLOAT16, seed=7, length_kind="uniform", lo=128, hi=4096)
+
 # Prefill: whole prompts of U[512, 4096] tokens; chunked prefill: the last 512
 # tokens of sequences of U[1024, 8192] tokens whose earlier tokens are cached.
 PREFILL = Workload(
@@ -122,7 +127,7 @@ CHUNKED_PREFILL = Workload(
     prefill="chunk", chunk=512)
 
 WORKLOADS = {w.name: w for w in (TINY, LLAMA3_8B, SHARED_PREFIX, LONG_CONTEXT, RAGGED,
-                                  PREFILL, CHUNKED_PREFILL)}
+                                  PREFILL, CHUNKED_PREFILL, MHA_7B)}
 
 
 # ----------------------------------------------------------------------------

@@ -99,8 +99,11 @@ def test_shapes_with_ragged_tails(pa, dtype, head_dim, bs):
 
 
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (32, 8), (64, 8), (32, 2), (24, 3),
-                                    (16, 1)])
+                                    (16, 1), (8, 1), (2, 2), (16, 2), (32, 32), (64, 32),
+                                    (16, 16), (64, 16), (48, 16)])
 def test_query_groupings(pa, hq, hkv):
+    """Every grouping the grouped kernel instantiates (1 to 32 KV heads per block:
+    multi-query, grouped and plain multi-head attention) and some it does not."""
     lens = [3, 70, 600, 1300]
     w = _small("llama3_8b", num_seqs=4, num_q_heads=hq, num_kv_heads=hkv, length_kind="fixed",
                lens=tuple(lens), seed=77 + hq + hkv)
@@ -281,3 +284,14 @@ def test_more_sequences_than_the_grouped_kernel_serves(pa):
     got = widen(DeviceBatch(batch).decode(pa))
     rows = list(range(0, 1100, 37)) + [1099]
     assert_close(got[rows], scenarios.decode_f64(batch, sequences=rows)[rows], "B=1100")
+
+
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 32, 16), (32, 32, 8), (8, 1, 32), (64, 16, 64)])
+def test_more_kv_heads_per_block_ragged(pa, hq, hkv, bs):
+    """Many KV heads per block mean few tokens per 128-row tile (4 for 32 heads),
+    so tiles split blocks; one KV head means a tile spans up to 16 blocks."""
+    w = _small("llama3_8b", num_seqs=6, num_q_heads=hq, num_kv_heads=hkv, block_size=bs,
+               length_kind="fixed", lens=(1, 5, 129, 700, 2049, 33), seed=5 + hq + bs)
+    batch = scenarios.fixed_batch(w)
+    got = widen(DeviceBatch(batch).decode(pa))
+    assert_close(got, scenarios.decode_f64(batch), f"Hq={hq} Hkv={hkv} bs={bs}")
