@@ -164,17 +164,27 @@ def gpu_uuid(torch, dev) -> str | None:
 # native arm
 # ----------------------------------------------------------------------------
 
-# the grouped decode kernel, its launch code and the headers it includes
-DECODE_SOURCES = ("pa_api.cu", "pa_decode_tcg.cu", "pa_common.cuh", "pa_internal.h",
-                  "pa_sm100.cuh")
+# The device code of the grouped decode kernel: its template, the parameter
+# struct it reads, and the device headers it includes (host-side launch code is
+# left out, so a change there keeps the recorded counters).
+DECODE_KERNEL_TEXT = (
+    ("pa_decode_tcg.cu", "template <int DT, int H, int G>\n__global__", "// Merge the partials"),
+    ("pa_internal.h", "struct DecodeParams {", "};"),
+    ("pa_common.cuh", None, None),
+    ("pa_sm100.cuh", None, None),
+)
 
 
 def kernel_sources_sha() -> str:
     csrc = os.path.join(ROOT, "paged_kv_cache_301_gb300", "csrc")
     h = hashlib.sha256()
-    for f in DECODE_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+    for f, start, end in DECODE_KERNEL_TEXT:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        if start is not None:
+            i = text.index(start)
+            text = text[i:text.index(end, i) + len(end)]
+        h.update(text.encode())
     return h.hexdigest()[:16]
 
 
