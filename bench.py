@@ -922,8 +922,10 @@ def main():
         ap.error("the prefill workloads run with --op prefill")
     if args.op != "decode":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "op": args.op,
-                              "unavailable": "no CPU arm for block moves"}), flush=True)
+            why = {"prefill": "the prefill line carries its oracle timing in cpu_baseline",
+                   "allocsim": "the allocator line times the oracle simulator itself"}.get(
+                       args.op, "no CPU arm for block moves")
+            print(json.dumps({"impl": "reference", "op": args.op, "unavailable": why}), flush=True)
         elif args.op == "allocsim":
             print(json.dumps(run_allocsim(args)), flush=True)
         elif args.op == "prefill":
