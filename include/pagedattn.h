@@ -304,7 +304,7 @@ pa_status pa_copy_blocks_multi(void* const* pools, int num_pools, const int32_t*
 
 /*
  * Block swap between GPU pools and pools in CPU RAM (the PagedAttention glossary
- * page, allocation and eviction: blocks of evicted sequences paged to CPU RAM).
+ * page, allocation and eviction: evicted blocks moved to host memory).
  * For every pair (src, dst) of block_pairs and every pool i < num_pools: block
  * dst of dst_pools[i] = block src of src_pools[i].  Swap-out passes GPU pools as
  * src and host pools as dst; swap-in the reverse; GPU-to-GPU also works.

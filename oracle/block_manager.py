@@ -66,7 +66,7 @@ class BlockManager:
             raise ValueError("n must be >= 0")
         have = len(self.free)
         if have < n:
-            raise OutOfBlocks(f"out of KV blocks: need {n}, have {have}")
+            raise OutOfBlocks(f"no free KV block left: need {n}, have {have}")
         cut = have - n
         taken = self.free[cut:]
         self.free = self.free[:cut]

@@ -18,7 +18,7 @@ pool per layer (subroutine-cs article §1, the bytes-per-token formula counts
 
 swap_blocks: blocks moved between two sets of pools, e.g. from the GPU pools to
 pools in CPU RAM and back (PagedAttention glossary page, allocation and eviction:
-blocks can be paged to CPU RAM).  Block dst of the destination pool i receives
+evicted blocks can move to host memory).  Block dst of the destination pool i receives
 block src of the source pool i.
 
 All work on raw uint16 storage bits, so results are exact bit copies.

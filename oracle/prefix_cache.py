@@ -69,7 +69,7 @@ class PrefixCachingBlockManager(BlockManager):
         if n < 0:
             raise ValueError("n must be >= 0")
         if len(self.free) + len(self.evictable) < n:
-            raise OutOfBlocks(f"out of KV blocks: need {n}, have "
+            raise OutOfBlocks(f"no free KV block left: need {n}, have "
                               f"{len(self.free)} free + {len(self.evictable)} evictable")
         while len(self.free) < n:
             b = self.evictable.pop(0)
@@ -122,7 +122,7 @@ class PrefixCachingBlockManager(BlockManager):
         need = self.blocks_needed(len(tokens)) - len(hits)
         queued = [b for b in hits if b not in self.refcount]
         if len(self.free) + len(self.evictable) - len(queued) < need:
-            raise OutOfBlocks(f"out of KV blocks: need {need} beyond the cached prefix")
+            raise OutOfBlocks(f"no free KV block left: need {need} beyond the cached prefix")
         for b in hits:
             if b in self.refcount:
                 self.refcount[b] += 1

@@ -23,7 +23,7 @@ ragged_steps   continuous-batching steps ("PagedAttention" glossary entry,
                batch decodes with the grown lengths.
 swap_round_trip  some sequences of a batch are evicted to a pool in CPU RAM
                (PagedAttention glossary entry, allocation and eviction: blocks
-               paged to CPU RAM), other work takes their GPU blocks, and the
+               moved to host memory), other work takes their GPU blocks, and the
                sequences come back into freshly allocated GPU blocks.
 
 Readings (listed in the design notes): the decode after a write attends to the

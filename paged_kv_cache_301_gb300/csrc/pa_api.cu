@@ -37,7 +37,7 @@ extern "C" const char* pa_status_string(int status) {
     case PA_ERR_WORKSPACE: return "workspace missing or too small";
     case PA_ERR_CUDA: return "CUDA error";
     case PA_ERR_BAD_BLOCK_ID: return "invalid block id, slot or sequence length in device data";
-    case PA_ERR_OUT_OF_BLOCKS: return "out of KV blocks";
+    case PA_ERR_OUT_OF_BLOCKS: return "no free KV block left";
     case PA_ERR_BLOCK_STATE: return "block or sequence in the wrong state";
     case PA_ERR_TIMEOUT: return "a kernel's bounded wait expired; results are incomplete";
     default: return "unknown status";

@@ -3,8 +3,8 @@
 //   pa_copy_blocks_multi  copy-on-write clones in the K and V pools of every
 //                         layer at once (one launch instead of one per layer);
 //   pa_swap_blocks        blocks between the GPU pools and pools in page-locked
-//                         host memory (the PagedAttention glossary page: blocks
-//                         of evicted sequences "paged to CPU RAM").
+//                         host memory (the PagedAttention glossary page names
+//                         moving evicted blocks to host memory as an extension).
 //
 // Both are the same gather/scatter: for every (src, dst) pair and every pool i,
 // block dst of dst_pools[i] receives the bytes of block src of src_pools[i].

@@ -26,8 +26,8 @@ def test_block_key_layout():
 def test_shared_system_prompt_arithmetic(bs):
     """N requests = a P-token system prompt + private suffixes: the floor(P/bs)
     full prompt blocks exist once with refcount N; every request after the first
-    skips exactly those tokens (the tutorial's "point at them (increment
-    refcount) instead of computing them")."""
+    skips exactly those tokens: shared blocks are referenced again, not
+    recomputed (tutorial §5, the relationship to prefix caching)."""
     g = np.random.default_rng(bs)
     P, N = 5 * bs + bs // 2, 6
     prompt = list(g.integers(0, 1000, size=P))
