@@ -168,7 +168,7 @@ def gpu_uuid(torch, dev) -> str | None:
 # struct it reads, and the device headers it includes (host-side launch code is
 # left out, so a change there keeps the recorded counters).
 DECODE_KERNEL_TEXT = (
-    ("pa_decode_tcg.cu", "template <int DT, int H, int G>\n__global__", "// Merge the partials"),
+    ("pa_decode_tcg.cu", "__device__ __forceinline__ int clamp_len", "// Merge the partials"),
     ("pa_internal.h", "struct DecodeParams {", "};"),
     ("pa_common.cuh", None, None),
     ("pa_sm100.cuh", None, None),
@@ -216,8 +216,10 @@ def decode_kernel_for(w, kernel: str) -> str:
 class NativeStep:
     """Device state of one replica: pool, tables, inputs; run() = one step."""
 
-    def __init__(self, pa, torch, w, dev, partition_tokens: int, kernel: str):
+    def __init__(self, pa, torch, w, dev, partition_tokens: int, kernel: str,
+                 fused: bool = True):
         self.pa, self.torch, self.w, self.dev = pa, torch, w, dev
+        self.fused = fused
         bs = w.block_size
         pairs = []
         if w.length_kind == "shared_prefix":
@@ -282,9 +284,10 @@ class NativeStep:
         # path) + combine when a sequence spans several partitions
         self.kernel = decode_kernel_for(w, kernel)
         # append_tokens, then decode: main + combine (grouped), plan + main
-        # (+ combine) (per-head), main (+ combine) (CUDA cores)
+        # (+ combine) (per-head), main (+ combine) (CUDA cores).  The fused step
+        # (pa_decode_append) writes the new tokens inside the grouped main kernel.
         if self.kernel == "tcg":
-            self.launches_per_step = 1 + 2
+            self.launches_per_step = (0 if fused else 1) + 2
         elif self.kernel == "tc_head":
             self.launches_per_step = 1 + 2 + (1 if P > 1 else 0)
         else:
@@ -320,13 +323,22 @@ class NativeStep:
         pa = self.pa
         if self.pairs is not None:
             pa.pa_copy_blocks(self.k_pool, self.v_pool, self.pairs)
-        pa.pa_append_tokens(self.k_pool, self.v_pool, self.key, self.value, self.tables,
-                            self.seq_lens)
+        if not self.fused:
+            pa.pa_append_tokens(self.k_pool, self.v_pool, self.key, self.value, self.tables,
+                                self.seq_lens)
 
     def decode(self):
-        self.pa.pa_decode(self.out, self.q, self.k_pool, self.v_pool, self.tables, self.seq_lens,
-                          self.w.scale, max_seq_len=self.max_seq_len,
-                          partition_tokens=self.pt, workspace=self.ws)
+        """The decode call; with `fused`, pa_decode_append, which also writes the
+        step's new tokens (inside the grouped kernel, else as a launch before it)."""
+        if self.fused:
+            self.pa.pa_decode_append(self.out, self.q, self.k_pool, self.v_pool, self.key,
+                                     self.value, self.tables, self.seq_lens, self.w.scale,
+                                     max_seq_len=self.max_seq_len, partition_tokens=self.pt,
+                                     workspace=self.ws)
+        else:
+            self.pa.pa_decode(self.out, self.q, self.k_pool, self.v_pool, self.tables,
+                              self.seq_lens, self.w.scale, max_seq_len=self.max_seq_len,
+                              partition_tokens=self.pt, workspace=self.ws)
 
     def run(self):
         self.write_step()
@@ -354,7 +366,8 @@ def run_native(args, dist_info):
         # before the first GPU call: the oracle's pool is a spawn pool anyway
         cpu_baseline = cpu_oracle_baseline(w, budget_s=args.cpu_budget)
     pa.set_decode_path(args.kernel)
-    step = NativeStep(pa, torch, w, dev, args.partition_tokens, args.kernel)
+    step = NativeStep(pa, torch, w, dev, args.partition_tokens, args.kernel,
+                      fused=not args.split_step)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -412,6 +425,8 @@ def run_native(args, dist_info):
     value = whole_job_gbs(kvb, world, ms_step)
     dec_avg_ms = sum(decode_ms) / len(decode_ms)
     dec_bytes = decode_bytes(step.lens, w, step.max_blocks)
+    if step.fused:     # the new tokens' K/V read once and written to the pool
+        dec_bytes += 4 * B * w.num_kv_heads * w.head_dim * w.elem_bytes
     peak, peak_kind = measured_peaks()
     achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
     traffic = recorded_traffic(w.name, step.kernel)
@@ -445,6 +460,8 @@ def run_native(args, dist_info):
             "decode_kernel": {"tcg": "tcgen05 + TMA, whole-block (decode_tcg_kernel)",
                               "tc_head": "tcgen05 + TMA, per KV head (decode_tc_kernel)",
                               "simt": "CUDA cores (decode_simt_kernel)"}[step.kernel],
+            "step": ("pa_decode_append: new tokens' cache write + decode in one call"
+                     if step.fused else "pa_append_tokens, then pa_decode"),
         },
         "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
         "unique_kv_gbs": round(whole_job_gbs(step.unique_tokens * w.num_kv_heads * w.head_dim * 4,
@@ -461,9 +478,13 @@ def run_native(args, dist_info):
         },
         "gpu_launches": step.launches_per_step * args.steps,
         "roofline": {
-            "kernel": {"tcg": "pa_decode (stream-K main + combine)",
-                       "tc_head": "pa_decode (plan + split-K main + combine)",
-                       "simt": "pa_decode (split-K main + combine)"}[step.kernel],
+            "kernel": ("pa_decode_append" if step.fused else "pa_decode") + " " +
+                      {"tcg": "(stream-K main + combine)" + (
+                          ", cache write inside the main kernel" if step.fused else ""),
+                       "tc_head": "(plan + split-K main + combine)" + (
+                           ", after the cache write" if step.fused else ""),
+                       "simt": "(split-K main + combine)" + (
+                           ", after the cache write" if step.fused else "")}[step.kernel],
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -906,6 +927,9 @@ def main():
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_head"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--split-step", action="store_true",
+                    help="decode step as pa_append_tokens + pa_decode instead of the one "
+                         "pa_decode_append call")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--op", choices=["decode", "swap", "cow_layers", "allocsim", "prefill"],
                     default="decode",

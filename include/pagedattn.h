@@ -244,6 +244,27 @@ pa_status pa_append_tokens(void* k_pool, void* v_pool, const void* key, const vo
                            int num_blocks, int dtype, int32_t* status_dev, cudaStream_t stream);
 
 /*
+ * One whole decode step: the cache write of pa_append_tokens (key / value
+ * packed [num_seqs, num_kv_heads, head_dim], no slot_mapping output), then
+ * pa_decode over the grown sequences ("10 — Paged Attention" tutorial, §4: the
+ * newest token gets its slot, then §5 "The kernel side": attention through the
+ * table).  Results and pools are bit-identical to those two calls in that
+ * order; the other arguments, the workspace and the error behaviour are those
+ * of pa_decode (key and value 16-byte aligned).  Where pa_decode runs its
+ * grouped tensor-core kernel, the write happens inside it: the CTA that reads a
+ * sequence's last tile stores the newest token before loading that tile, which
+ * saves one launch per step.  The block receiving a sequence's newest token must
+ * not be in another sequence's table (copy-on-write it first, as for any write).
+ */
+pa_status pa_decode_append(void* out, const void* q, void* k_pool, void* v_pool,
+                           const void* key, const void* value, const int32_t* block_tables,
+                           const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                           int num_blocks, int max_seq_len, float scale, int dtype,
+                           int partition_tokens, void* workspace, size_t workspace_bytes,
+                           int32_t* status_dev, cudaStream_t stream);
+
+/*
  * Paged multi-query attention with a causal mask: prefill, chunked prefill and
  * verification of several drafted tokens (subroutine-cs article, introduction:
  * the prefill phase computes all prompt tokens at once; "10 — Paged Attention"

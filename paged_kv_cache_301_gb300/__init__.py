@@ -100,6 +100,31 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: 
     return out
 
 
+def pa_decode_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                     v_pool: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                     block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                     max_seq_len: Optional[int] = None, partition_tokens: int = 0,
+                     workspace: Optional[torch.Tensor] = None,
+                     status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step (see include/pagedattn.h, pa_decode_append): the newest
+    token of every sequence (key/value [B, Hkv, D]) goes to its slot, then decode
+    attention over the grown sequences, as pa_append_tokens + pa_decode."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, Dk = k_pool.shape
+    MB = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = MB * bs
+    if workspace is None:
+        workspace = alloc_workspace(B, Hq, D, max_seq_len, partition_tokens, q.device)
+    st = lib().pa_decode_append(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(key), _ptr(value),
+        _ptr(block_tables), _ptr(seq_lens), B, Hq, Hkv, D, bs, MB, NB, int(max_seq_len),
+        float(scale), _dtype(q), int(partition_tokens), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream(stream))
+    _check(st, "pa_decode_append")
+    return out
+
+
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -399,7 +424,8 @@ class BlockManager:
 
 
 __all__ = [
-    "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_workspace_bytes",
+    "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_append",
+    "pa_decode_workspace_bytes",
     "pa_decode_noalloc", "set_decode_path",
     "alloc_workspace", "pa_reshape_and_cache", "pa_append_tokens", "pa_prefill", "set_prefill_path",
     "pa_copy_blocks_multi", "pa_swap_blocks", "pa_copy_blocks", "pa_decode_slots",

@@ -56,13 +56,17 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int h
   return workspace_layout(num_seqs, num_q_heads, head_dim, P).total;
 }
 
-extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
-                               const int32_t* block_tables, const int32_t* seq_lens,
-                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                               int block_size, int max_blocks, int num_blocks, int max_seq_len,
-                               float scale, int dtype, int partition_tokens, void* workspace,
-                               size_t workspace_bytes, int32_t* status_dev,
-                               cudaStream_t stream) {
+// pa_decode, optionally preceded by the decode-step cache write of
+// pa_append_tokens (new_k / new_v non-null): fused into the grouped tensor-core
+// kernel where that kernel runs, two launches otherwise.  Every argument is
+// checked before anything is launched.
+static pa_status decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool,
+                             const void* new_k, const void* new_v,
+                             const int32_t* block_tables, const int32_t* seq_lens,
+                             int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_blocks, int num_blocks, int max_seq_len,
+                             float scale, int dtype, int partition_tokens, void* workspace,
+                             size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks <= 0 ||
       num_blocks <= 0 || max_seq_len < 0)
     return PA_ERR_INVALID_ARG;
@@ -78,6 +82,9 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
   if ((((uintptr_t)out | (uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool) & 15u) != 0)
+    return PA_ERR_INVALID_ARG;
+  const bool append = new_k != nullptr || new_v != nullptr;
+  if (append && (!new_k || !new_v || (((uintptr_t)new_k | (uintptr_t)new_v) & 15u) != 0))
     return PA_ERR_INVALID_ARG;
   const int P = max(1, num_partitions(max_seq_len, pt));
   const WorkspaceLayout wl = workspace_layout(num_seqs, num_q_heads, head_dim, P);
@@ -108,13 +115,25 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   p.ws_l = reinterpret_cast<float*>(ws + wl.l_off);
   p.ws_acc = reinterpret_cast<float*>(ws + wl.acc_off);
   p.status_dev = status_dev;
+  p.new_k = nullptr;
+  p.new_v = nullptr;
 
   const int path = g_decode_path;
   const bool grouped = path != PA_DECODE_SIMT && path != PA_DECODE_TC_HEAD && tcg_supported(p);
-  if (grouped) return launch_decode_tcg(p, ws + wl.sk_off, stream);
+  if (grouped) {
+    p.new_k = new_k;
+    p.new_v = new_v;
+    return launch_decode_tcg(p, ws + wl.sk_off, stream);
+  }
   const bool per_head = path != PA_DECODE_SIMT && tc_supported(p);
   if ((path == PA_DECODE_TC || path == PA_DECODE_TC_HEAD) && !per_head) return PA_ERR_UNSUPPORTED;
   pa_status st;
+  if (append) {
+    st = pa_append_tokens(const_cast<void*>(k_pool), const_cast<void*>(v_pool), new_k, new_v,
+                          block_tables, seq_lens, nullptr, num_seqs, 0, num_kv_heads, head_dim,
+                          block_size, max_blocks, num_blocks, dtype, status_dev, stream);
+    if (st != PA_OK) return st;
+  }
   if (per_head) {
     st = launch_decode_tc(p, reinterpret_cast<int2*>(ws + wl.items_off),
                           reinterpret_cast<int*>(ws + wl.queue_off), stream);
@@ -123,6 +142,35 @@ extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, con
   }
   if (st != PA_OK || P == 1) return st;
   return launch_combine(p, stream);
+}
+
+extern "C" pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, int max_blocks, int num_blocks, int max_seq_len,
+                               float scale, int dtype, int partition_tokens, void* workspace,
+                               size_t workspace_bytes, int32_t* status_dev,
+                               cudaStream_t stream) {
+  return decode_impl(out, q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, max_blocks, num_blocks,
+                     max_seq_len, scale, dtype, partition_tokens, workspace, workspace_bytes,
+                     status_dev, stream);
+}
+
+extern "C" pa_status pa_decode_append(void* out, const void* q, void* k_pool, void* v_pool,
+                                      const void* key, const void* value,
+                                      const int32_t* block_tables, const int32_t* seq_lens,
+                                      int num_seqs, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int max_blocks,
+                                      int num_blocks, int max_seq_len, float scale, int dtype,
+                                      int partition_tokens, void* workspace,
+                                      size_t workspace_bytes, int32_t* status_dev,
+                                      cudaStream_t stream) {
+  if (num_seqs > 0 && (!key || !value)) return PA_ERR_INVALID_ARG;
+  return decode_impl(out, q, k_pool, v_pool, key, value, block_tables, seq_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, max_blocks, num_blocks,
+                     max_seq_len, scale, dtype, partition_tokens, workspace, workspace_bytes,
+                     status_dev, stream);
 }
 
 extern "C" pa_status pa_set_decode_path(int path) {

@@ -91,6 +91,7 @@ struct Tail {
   uint64_t p_full[2], p_empty[2];
   uint64_t o_full[2], o_empty[2];
   uint64_t red[2], lsum, drain;
+  uint64_t app_done;          // newest tokens of this CTA's sequences are in the pool
   SegInfo seg[2];
   float red_buf[2][4][N];
   float alpha[2][N];
@@ -123,6 +124,33 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
 // First tile of CTA c's range (T tiles over `grid` CTAs; c * T < 2^31 here).
 __device__ __forceinline__ int range_start(int c, int T, int grid) {
   return (int)((unsigned)c * (unsigned)T / (unsigned)grid);
+}
+
+// Decode-step cache write of sequence b, vectors first, first + stride, ...:
+// the K/V rows of token L - 1 (all H heads, 16-byte vectors) go to its slot
+// table[(L-1) / bs] * bs + (L-1) % bs ("10 — Paged Attention" tutorial, §4
+// PhysicalIndex).  L <= 0 or past the table writes nothing (the length check
+// reports it); a block id outside the pool is reported and skipped.
+template <int H>
+__device__ __forceinline__ void store_newest(const DecodeParams& p, int b, int first, int stride) {
+  constexpr int kRowVecs = H * kD * 2 / 16;
+  const int L = p.seq_lens[b];
+  if (L <= 0 || L > p.max_blocks * p.bs) return;
+  const int pos = L - 1;
+  const int32_t id = p.block_tables[(int64_t)b * p.max_blocks + pos / p.bs];
+  if (id < 0 || id >= p.num_blocks) {
+    if (first == 0) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+    return;
+  }
+  const int64_t dst = ((int64_t)id * p.bs + pos % p.bs) * kRowVecs;
+  const uint4* sk = static_cast<const uint4*>(p.new_k) + (int64_t)b * kRowVecs;
+  const uint4* sv = static_cast<const uint4*>(p.new_v) + (int64_t)b * kRowVecs;
+  uint4* dk = static_cast<uint4*>(const_cast<void*>(p.k_pool)) + dst;
+  uint4* dv = static_cast<uint4*>(const_cast<void*>(p.v_pool)) + dst;
+  for (int v = first; v < kRowVecs; v += stride) {
+    dk[v] = sk[v];
+    dv[v] = sv[v];
+  }
 }
 
 template <int DT, int H, int G>
@@ -163,6 +191,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     mbar_init(&tl->lsum, 4);
     mbar_init(&tl->drain, 1);
+    mbar_init(&tl->app_done, 128);
     tl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -211,6 +240,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (L == 0 && b % grid == c) {
         uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)b * p.Hq * kD;
         for (int e = 0; e < p.Hq * kD; ++e) o[e] = 0;
+        if (p.new_k != nullptr) store_newest<H>(p, b, 0, 1);   // no tile reads it
       }
       run += (L + TT - 1) / TT;
     }
@@ -224,6 +254,24 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
   tc_fence_after();
   const int T = tl->prefix[p.B];
   const int t_begin = range_start(c, T, grid), t_end = range_start(c + 1, T, grid);
+  if (warp >= 2) {
+    // Decode-step cache write: the newest token of a sequence lies in its last
+    // tile, and tiles cover disjoint token ranges, so the CTA whose range holds
+    // that tile stores the token.  The writes are fenced against the async
+    // proxy; the producer waits for app_done before it loads such a tile.
+    if (p.new_k != nullptr && t_begin < t_end) {
+      int lo = 0, hi = p.B;            // first sequence whose last tile is >= t_begin
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (tl->prefix[mid + 1] > t_begin) hi = mid;
+        else lo = mid + 1;
+      }
+      for (int b = lo; b < p.B && tl->prefix[b + 1] <= t_end; ++b)
+        if (tl->prefix[b + 1] > tl->prefix[b]) store_newest<H>(p, b, threadIdx.x - 64, 128);
+    }
+    fence_async_global();
+    mbar_arrive(&tl->app_done);
+  }
   // Ring order follows the MMA's consumption order: K(0), then for t >= 1 K(t)
   // before V(t-1), and V(last) at the end.  Positions in that sequence:
   const int t_last = t_end - t_begin - 1;
@@ -247,6 +295,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     int q_issued[2] = {-1, -1};
     int seg_idx = 0;
     bool ok = true;
+    bool appended = p.new_k == nullptr;   // newest tokens already in the pool
     int tile = t_begin;
     // V tile of the previous K tile, issued after the next K tile
     bool pend = false;
@@ -354,6 +403,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         return id;
       };
       int32_t cur = load_chunk(kb), nxt = load_chunk(kb + 32);
+      const int seq_tiles = tl->prefix[sg.b + 1] - tl->prefix[sg.b];
       for (int j = sg.j0; j < sg.j1 && ok; ++j) {
         const int tok0 = j * TT;
         int k0, nops, box_tokens, tok_off;
@@ -377,6 +427,16 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int32_t a = __shfl_sync(0xFFFFFFFFu, cur, src & 31);
         const int32_t bb = __shfl_sync(0xFFFFFFFFu, nxt, src & 31);
         const int32_t blk = src < 32 ? a : bb;
+        if (!appended && j == seq_tiles - 1) {   // holds the newest token: wait for its write
+          bool good = mbar_wait(&tl->app_done, 0, abort_flag, kWaitNs);
+          good = __all_sync(0xFFFFFFFFu, good);
+          if (!good) {
+            if (lane == 0) set_abort();
+            ok = false;
+            break;
+          }
+          appended = true;
+        }
         ok = issue(&tm_k, nops, box_tokens, tok_off, blk);
         if (ok && pend) ok = issue(&tm_v, pend_nops, pend_box, pend_off, pend_blk);
         pend = true;

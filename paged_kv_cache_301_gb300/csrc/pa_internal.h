@@ -25,6 +25,11 @@ struct DecodeParams {
   float* ws_l;           // [B, Hq, P] sum of exp2(s - m) per partition
   float* ws_acc;         // [B, Hq, P, D] unnormalised partial outputs
   int32_t* status_dev;   // nullable: checked mode
+  // Decode-step cache write done inside the grouped kernel (both null: none).
+  // new_k[b] / new_v[b] ([Hkv, D], packed) become the pool rows of token
+  // seq_lens[b] - 1 before any load of that token's tile.
+  const void* new_k;
+  const void* new_v;
 };
 
 // Workspace carve-up; identical for every decode kernel.
