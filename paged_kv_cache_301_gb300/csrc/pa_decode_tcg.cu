@@ -79,7 +79,7 @@ struct Geo {
 struct SegInfo {
   int b, L, j0, j1;       // sequence, its length, tile range [j0, j1) within it
   int direct, slot;       // direct output, or partial slot 0/1 of this CTA
-  int valid, pad;
+  int valid, last;        // last: the CTA's final segment
 };
 
 template <int N>
@@ -92,6 +92,9 @@ struct Tail {
   uint64_t o_full[2], o_empty[2];
   uint64_t red[2], lsum, drain;
   uint64_t app_done;          // newest tokens of this CTA's sequences are in the pool
+  uint64_t staged;            // final outputs staged in the ring (one arrive per softmax warp)
+  uint64_t p_staged[2];       // a segment's outputs staged in P' buffer i (one arrive per softmax warp)
+  uint64_t p_released[2];     // the bulk copy has read P' buffer i
   SegInfo seg[2];
   float red_buf[2][4][N];
   float alpha[2][N];
@@ -192,6 +195,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     mbar_init(&tl->lsum, 4);
     mbar_init(&tl->drain, 1);
     mbar_init(&tl->app_done, 128);
+    mbar_init(&tl->staged, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tl->p_staged[i], 4);
+      mbar_init(&tl->p_released[i], 1);
+    }
     tl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -299,11 +307,14 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     int tile = t_begin;
     // V tile of the previous K tile, issued after the next K tile
     bool pend = false;
-    int pend_nops = 0, pend_box = 0, pend_off = 0;
+    int pend_nbox = 0, pend_box = 0, pend_tok = 0;
     int32_t pend_blk = 0;
-    auto issue = [&](const CUtensorMap* map, int nops, int box_tokens, int tok_off,
+    // One tile: lanes < nbox each copy one box of box_tokens tokens x H heads,
+    // lane i at (token-in-block tok, block blk) of the [blocks][bs][H][D] pool;
+    // the boxes fill the stage (nbox * box_tokens = TT tokens).
+    auto issue = [&](const CUtensorMap* map, int nbox, int box_tokens, int tok,
                      int32_t blk) -> bool {
-      const uint32_t bytes = (uint32_t)nops * box_tokens * H * 128u * 2u;
+      const uint32_t bytes = (uint32_t)nbox * box_tokens * H * 128u * 2u;
       bool good = true;
       if (lane == 0) {
         good = mbar_wait(&tl->empty[stage], sphase ^ 1, abort_flag, kWaitNs);
@@ -312,11 +323,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       good = __shfl_sync(0xFFFFFFFFu, (int)good, 0) != 0;
       if (!good) return false;
-      if (lane < nops) {
+      if (lane < nbox) {
         uint8_t* dst = smem + Gm::kRingOff + stage * kStage + lane * box_tokens * H * 128;
-        const int row = blk * p.bs + tok_off;
-        tma_load_3d_hint(dst, map, &tl->full[stage], 0, 0, row, policy);
-        tma_load_3d_hint(dst + kSlab, map, &tl->full[stage], 64, 0, row, policy);
+        tma_load_4d_hint(dst, map, &tl->full[stage], 0, 0, tok, blk, policy);
+        tma_load_4d_hint(dst + kSlab, map, &tl->full[stage], 64, 0, tok, blk, policy);
       }
       issued[stage] = sphase;
       if (++stage == S) {
@@ -325,6 +335,17 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       return true;
     };
+    // Block ids of a segment, 32 per chunk held one per lane (ids past the
+    // sequence's blocks are loaded but never used).  A segment's length and first
+    // two chunks are loaded while the previous segment streams: waiting for those
+    // dependent loads at the segment start left the ring without new copies for
+    // their latency (measured on GB300: ~4 us per segment boundary).
+    auto raw_ids = [&](int bb, int base) -> int32_t {
+      const int k = base + lane;
+      return k < p.max_blocks ? p.block_tables[(int64_t)bb * p.max_blocks + k] : 0;
+    };
+    int pf_b = -1, pf_len = 0;
+    int32_t pf_cur = 0, pf_nxt = 0;
     int b = 0;
     if (t_begin < t_end) {        // the sequence holding this CTA's first tile
       int lo = 0, hi = p.B - 1;
@@ -348,15 +369,23 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
           ++b;
         }
         sg.b = b;
-        sg.L = clamp_len(p, b);
+        if (pf_b != b) {                 // first segment: nothing prefetched
+          pf_b = b;
+          pf_len = p.seq_lens[b];
+          const int kf = ((tile - tpb) * TT) / p.bs;
+          pf_cur = raw_ids(b, kf);
+          pf_nxt = raw_ids(b, kf + 32);
+        }
+        sg.L = pf_len < 0 ? 0 : (pf_len > p.max_seq_len ? p.max_seq_len : pf_len);
         sg.j0 = tile - tpb;
         sg.j1 = min(t_end, tpb1) - tpb;
         sg.direct = (sg.j0 == 0 && sg.j1 == tpb1 - tpb);
         sg.slot = seg_idx == 0 ? 0 : 1;
         sg.valid = 1;
+        sg.last = tpb1 >= t_end;
       }
       if (!sg.valid && pend) {           // the last V tile of this CTA
-        ok = issue(&tm_v, pend_nops, pend_box, pend_off, pend_blk);
+        ok = issue(&tm_v, pend_nbox, pend_box, pend_tok, pend_blk);
         pend = false;
         if (!ok) break;
       }
@@ -388,45 +417,53 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
       if (!ok) break;
-      // block ids of this segment, 32 per chunk held one per lane, next chunk prefetched
-      const int32_t* table = p.block_tables + (int64_t)sg.b * p.max_blocks;
       const int nblk_seq = (sg.L + p.bs - 1) / p.bs;
-      const int k_first = (sg.j0 * TT) / p.bs;
-      int kb = k_first;
-      auto load_chunk = [&](int base) -> int32_t {
-        const int k = base + lane;
-        int32_t id = 0;
-        if (k < nblk_seq) {
-          id = table[k];
-          if (p.status_dev && (id < 0 || id >= p.num_blocks)) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
-        }
-        return id;
-      };
-      int32_t cur = load_chunk(kb), nxt = load_chunk(kb + 32);
+      int kb = (sg.j0 * TT) / p.bs;
+      int32_t cur = pf_cur, nxt = pf_nxt;
       const int seq_tiles = tl->prefix[sg.b + 1] - tl->prefix[sg.b];
+      if (tl->prefix[sg.b] + sg.j1 < t_end) {   // the next segment: the next sequence with tiles
+        int nb = sg.b + 1;
+        while (tl->prefix[nb + 1] == tl->prefix[nb]) ++nb;
+        pf_b = nb;
+        pf_len = p.seq_lens[nb];
+        pf_cur = raw_ids(nb, 0);
+        pf_nxt = raw_ids(nb, 32);
+      }
       for (int j = sg.j0; j < sg.j1 && ok; ++j) {
+        // boxes of the tile: TT / bs whole blocks, or one TT-token piece of a block
         const int tok0 = j * TT;
-        int k0, nops, box_tokens, tok_off;
-        if (TT >= p.bs) {
-          k0 = tok0 / p.bs;
-          nops = min(TT / p.bs, nblk_seq - k0);
-          box_tokens = p.bs;
-          tok_off = 0;
-        } else {
-          k0 = tok0 / p.bs;
-          nops = 1;
-          box_tokens = TT;
-          tok_off = tok0 % p.bs;
-        }
+        const int box_tokens = TT >= p.bs ? p.bs : TT;
+        const int nbox = TT / box_tokens;
+        const int k0 = tok0 / p.bs;
+        const int tok_off = TT >= p.bs ? 0 : tok0 % p.bs;
+        // The box holding the sequence's last token is shifted back by sh rows so
+        // that it ends at that token: its first sh rows read a negative in-block
+        // coordinate (zeros) or the sequence's earlier tokens.  Boxes after it
+        // read block -1 (zeros).  Every row is finite and the softmax masks the
+        // rows that are not this tile's tokens, so no copy has to be waited for
+        // to clean rows.
+        const int n_valid = sg.L - tok0;
+        const int il = n_valid >= TT ? nbox : (n_valid - 1) / box_tokens;
+        const int sh = n_valid >= TT ? 0 : box_tokens - (n_valid - il * box_tokens);
         while (k0 - kb >= 32) {          // advance the id window
           kb += 32;
           cur = nxt;
-          nxt = load_chunk(kb + 32);
+          nxt = raw_ids(sg.b, kb + 32);
         }
-        const int src = k0 + (lane < nops ? lane : 0) - kb;
+        const int src = min(k0 + lane, nblk_seq - 1) - kb;     // < 64: nbox <= 16
         const int32_t a = __shfl_sync(0xFFFFFFFFu, cur, src & 31);
         const int32_t bb = __shfl_sync(0xFFFFFFFFu, nxt, src & 31);
-        const int32_t blk = src < 32 ? a : bb;
+        int32_t blk = src < 32 ? a : bb;
+        int tok = tok_off;
+        if (lane > il) {
+          blk = -1;
+        } else {
+          if (lane == il) tok = tok_off - sh;
+          if (blk < 0 || blk >= p.num_blocks) {   // outside the pool: the copy reads zeros
+            if (lane < nbox) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+            blk = p.num_blocks;
+          }
+        }
         if (!appended && j == seq_tiles - 1) {   // holds the newest token: wait for its write
           bool good = mbar_wait(&tl->app_done, 0, abort_flag, kWaitNs);
           good = __all_sync(0xFFFFFFFFu, good);
@@ -437,12 +474,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
           }
           appended = true;
         }
-        ok = issue(&tm_k, nops, box_tokens, tok_off, blk);
-        if (ok && pend) ok = issue(&tm_v, pend_nops, pend_box, pend_off, pend_blk);
+        ok = issue(&tm_k, nbox, box_tokens, tok, blk);
+        if (ok && pend) ok = issue(&tm_v, pend_nbox, pend_box, pend_tok, pend_blk);
         pend = true;
-        pend_nops = nops;
+        pend_nbox = nbox;
         pend_box = box_tokens;
-        pend_off = tok_off;
+        pend_tok = tok;
         pend_blk = blk;
       }
       if (!ok) break;
@@ -564,6 +601,39 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       const bool w = mbar_wait(bar, parity, abort_flag, kWaitNs);
       return __all_sync(0xFFFFFFFFu, w);
     };
+    // A segment's outputs leave through the TMA unit.  Global stores issued by
+    // these warps while the TMA copies keep the memory system saturated stall
+    // each warp ~190 cycles per store on GB300 (~3 us per segment, in a burst
+    // or spread over the following tiles alike).  So the outputs are written to
+    // shared memory and sent with one bulk copy: the CTA's final segment stages
+    // them in the idle ring; another segment (N <= 32, two P' buffers) in the
+    // P' buffer of its last tile, which its P'.V has finished reading and which
+    // the next tile does not use.  Before that buffer takes a P' again, the bulk
+    // copy must have read it and each thread re-zeroes its row (P' relies on
+    // zeros off the block diagonal).  For N = 64 (one P' buffer; few segments
+    // per CTA in its batches) other segments store directly.
+    constexpr bool kStageP = Gm::kPBufs == 2;
+    int stg_pend = 0;                  // bit i: P' buffer i holds staged outputs
+    int stg_phase = 0;                 // bit i: parity of P' buffer i's next staging
+    auto release_p = [&](int ps) -> bool {
+      if (!(stg_pend >> ps & 1)) return true;
+      if (threadIdx.x == 64) {
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        mbar_arrive(&tl->p_released[ps]);
+      }
+      if (!wait_all(&tl->p_released[ps], stg_phase >> ps & 1)) return false;
+      uint8_t* pb = smem + Gm::kPOff + ps * Gm::kPBytes + (r >> 6) * (N * 128);
+      const int chunk = (r & 63) >> 3;
+#pragma unroll
+      for (int q = 0; q < N; ++q) {
+        const int off = q * 128 + ((chunk ^ (q & 7)) << 4) + (r & 7) * 2;
+        *reinterpret_cast<uint16_t*>(pb + off) = 0;
+        *reinterpret_cast<uint16_t*>(pb + Gm::kPHalf + off) = 0;
+      }
+      stg_pend &= ~(1 << ps);
+      stg_phase ^= 1 << ps;
+      return true;
+    };
     for (;;) {
       const int islot = seg_idx & 1;
       if (!wait_all(&tl->seg_full[islot], (seg_idx >> 1) & 1)) { ok = false; break; }
@@ -623,7 +693,20 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->s_empty[slot]);
-        const bool valid = (sg.j0 + j) * TT + tt < sg.L;
+        // rows of this tile's tokens: all rows of an interior tile; in a
+        // sequence's last tile the boxes before the last one and the last box's
+        // rows from its shift on (the producer's layout of that tile)
+        bool valid = true;
+        {
+          const int n_valid = sg.L - (sg.j0 + j) * TT;
+          if (n_valid < TT) {
+            const int bx = TT >= p.bs ? p.bs : TT;
+            const int il = (n_valid - 1) / bx;
+            const int sh = bx - (n_valid - il * bx);
+            const int ib = tt / bx;
+            valid = ib < il || (ib == il && tt - ib * bx >= sh);
+          }
+        }
         float wm[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -661,6 +744,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         // P' entries of this row: (head h*G+g, column r)
         const int ps = t % Gm::kPBufs, pph = (t / Gm::kPBufs) & 1;
         if (!wait_all(&tl->p_empty[ps], pph ^ 1)) { ok = false; break; }
+        if (kStageP && !release_p(ps)) { ok = false; break; }
         uint8_t* pbuf = smem + Gm::kPOff + ps * Gm::kPBytes + (r >> 6) * (N * 128);
         const int chunk = (r & 63) >> 3;
 #pragma unroll
@@ -671,22 +755,6 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
           const int off = q * 128 + ((chunk ^ (q & 7)) << 4) + (r & 7) * 2;
           *reinterpret_cast<uint16_t*>(pbuf + off) = hi;
           *reinterpret_cast<uint16_t*>(pbuf + Gm::kPHalf + off) = lo;
-        }
-        // rows of tokens past the end: zero their V row (0 * garbage must not reach O)
-        if ((sg.j0 + j + 1) * TT > sg.L) {
-          const int u = pos_v(t);
-          const int vs = u % S, vph = (u / S) & 1;
-          if (!wait_all(&tl->full[vs], vph)) { ok = false; break; }
-          if (!valid) {
-            uint4* r0 = reinterpret_cast<uint4*>(smem + Gm::kRingOff + vs * kStage + r * 128);
-            uint4* r1 = reinterpret_cast<uint4*>(smem + Gm::kRingOff + vs * kStage + kSlab + r * 128);
-            const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              r0[i] = z;
-              r1[i] = z;
-            }
-          }
         }
         fence_async_smem();
         __syncwarp();
@@ -717,25 +785,76 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       if (!accumulate(tile_g + ntiles - 1, round - 1)) { ok = false; break; }
       const int Hq = p.Hq;
+      // direct: normalised output; partial: the unnormalised accumulator, with
+      // its (max, sum) per query head stored by the lanes of one warp.  The
+      // division is the fast one (at most 2 ulp in fp32 for l in [1, 2^31], far
+      // below the output's storage rounding): the IEEE one, with its slow-path
+      // branch per element, cost ~2.3 us per segment on GB300.
 #pragma unroll
       for (int q = 0; q < N; ++q) {
-        if (q < Hq) {
+        if (q < Hq && sg.direct) {
           const float l = tl->lred[0][q] + tl->lred[1][q] + tl->lred[2][q] + tl->lred[3][q];
-          if (sg.direct) {
-            static_cast<uint16_t*>(p.out)[((int64_t)sg.b * Hq + q) * kD + r] = narrow<DT>(acc[q] / l);
-          } else {
-            const int64_t idx = ((int64_t)c * 2 + sg.slot) * Hq + q;
-            sp.part_acc[idx * kD + r] = acc[q];
-            if (r == 0) {
-              sp.part_m[idx] = tl->m_fin[q];
-              sp.part_l[idx] = l;
+          acc[q] = __fdividef(acc[q], l);
+        }
+      }
+      const int64_t part0 = ((int64_t)c * 2 + sg.slot) * Hq;   // partial index of head 0
+      if (!sg.direct && wq == 0) {
+        for (int q = lane; q < Hq; q += 32) {
+          sp.part_m[part0 + q] = tl->m_fin[q];
+          sp.part_l[part0 + q] = tl->lred[0][q] + tl->lred[1][q] + tl->lred[2][q] + tl->lred[3][q];
+        }
+      }
+      const int64_t out0 = sg.direct ? (int64_t)sg.b * Hq * kD : part0 * kD;
+      const int last_ps = (tile_g + ntiles - 1) % Gm::kPBufs;
+      if (sg.last || kStageP) {
+        // final segment: every MMA has completed and every copy has landed, the
+        // ring is idle; otherwise the P' buffer of the segment's last tile
+        uint8_t* stg = sg.last ? smem + Gm::kRingOff : smem + Gm::kPOff + last_ps * Gm::kPBytes;
+        uint64_t* bar = sg.last ? &tl->staged : &tl->p_staged[last_ps];
+        const int par = sg.last ? 0 : (stg_phase >> last_ps & 1);
+#pragma unroll
+        for (int q = 0; q < N; ++q) {
+          if (q < Hq) {
+            if (sg.direct) reinterpret_cast<uint16_t*>(stg)[q * kD + r] = narrow<DT>(acc[q]);
+            else reinterpret_cast<float*>(stg)[q * kD + r] = acc[q];
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+        if (threadIdx.x == 64) {
+          if (mbar_wait(bar, par, abort_flag, kWaitNs)) {
+            void* dst = sg.direct ? static_cast<void*>(static_cast<uint16_t*>(p.out) + out0)
+                                  : static_cast<void*>(sp.part_acc + out0);
+            const uint32_t bytes = (uint32_t)Hq * kD * (sg.direct ? 2u : 4u);
+            if (sg.last) {
+              bulk_store_and_release(dst, stg, bytes);
+            } else {
+              asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                           "r"(smem_addr(stg)), "r"(bytes)
+                           : "memory");
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
+          } else {
+            ok = false;
+          }
+        }
+        if (!sg.last) stg_pend |= 1 << last_ps;
+        ok = __all_sync(0xFFFFFFFFu, ok);    // one lane's failed wait ends the warp's loop
+        if (!ok) break;
+      } else {
+#pragma unroll
+        for (int q = 0; q < N; ++q) {
+          if (q < Hq) {
+            if (sg.direct) static_cast<uint16_t*>(p.out)[out0 + (int64_t)q * kD + r] = narrow<DT>(acc[q]);
+            else sp.part_acc[out0 + (int64_t)q * kD + r] = acc[q];
           }
         }
       }
       tile_g += ntiles;
       ++seg_idx;
     }
+    if (threadIdx.x == 64) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     if (!ok) set_abort();
   }
 
@@ -913,7 +1032,8 @@ bool tcg_supported(const DecodeParams& p) {
   if (p.B > kMaxSeqs) return false;
   if (G != 1 && G != 2 && G != 4 && G != 8) return false;
   if (p.Hq > kMaxHq) return false;
-  if ((long long)p.num_blocks * p.bs >= (1ll << 31)) return false;
+  // a bad block id is redirected to row num_blocks * bs (+ offset < 64): stays an int
+  if ((long long)p.num_blocks * p.bs + 64 >= (1ll << 31)) return false;
   if ((long long)p.B * p.Hq >= (1ll << 31)) return false;
   return encode_fn() != nullptr;
 }
@@ -940,15 +1060,19 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
       p.dtype == PA_BFLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int box_tokens = p.bs < TT ? p.bs : TT;
   CUtensorMap tk, tv, tq;
-  const cuuint64_t kv_dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)p.num_blocks * p.bs};
-  const cuuint64_t kv_strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-  const cuuint32_t kv_box[3] = {64, (cuuint32_t)H, (cuuint32_t)box_tokens};
-  const cuuint32_t ones[3] = {1, 1, 1};
-  if (enc(&tk, dt, 3, const_cast<void*>(p.k_pool), kv_dims, kv_strides, kv_box, ones,
+  // [blocks][bs][H][D] as a 4-D tensor: a box whose in-block coordinate is
+  // negative reads zeros there instead of the previous block's tokens
+  const cuuint64_t kv_dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)p.bs,
+                                 (cuuint64_t)p.num_blocks};
+  const cuuint64_t kv_strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2,
+                                    (cuuint64_t)p.bs * H * kD * 2};
+  const cuuint32_t kv_box[4] = {64, (cuuint32_t)H, (cuuint32_t)box_tokens, 1};
+  const cuuint32_t ones[4] = {1, 1, 1, 1};
+  if (enc(&tk, dt, 4, const_cast<void*>(p.k_pool), kv_dims, kv_strides, kv_box, ones,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return PA_ERR_INVALID_ARG;
-  if (enc(&tv, dt, 3, const_cast<void*>(p.v_pool), kv_dims, kv_strides, kv_box, ones,
+  if (enc(&tv, dt, 4, const_cast<void*>(p.v_pool), kv_dims, kv_strides, kv_box, ones,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return PA_ERR_INVALID_ARG;

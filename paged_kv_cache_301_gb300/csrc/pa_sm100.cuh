@@ -90,6 +90,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 4-D tile load with an L2 eviction-priority hint.
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* map,
+                                                 uint64_t* bar, int c0, int c1, int c2, int c3,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "l"(policy)
+      : "memory");
+}
+
 // 3-D tile load with an L2 eviction-priority hint.
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map,
                                                  uint64_t* bar, int c0, int c1, int c2,
@@ -319,6 +331,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // Named barrier for `count` threads (a multiple of 32) of the CTA.
+// Bulk copy shared -> global by the TMA unit (both addresses 16-byte aligned,
+// bytes a multiple of 16), committed as one bulk group; then wait until the
+// unit has read the shared source (the global writes complete asynchronously
+// and are visible to later kernels of the stream).
+__device__ __forceinline__ void bulk_store_and_release(void* gdst, const void* ssrc,
+                                                       uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_addr(ssrc)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
