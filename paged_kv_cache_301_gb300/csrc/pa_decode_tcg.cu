@@ -867,15 +867,17 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
 }
 
 // Merge the partials of sequences cut by CTA range boundaries.  One warp per
-// (sequence, query head): lanes read the parts' (max, sum) in parallel, then
-// the accumulators are summed with the per-part weights, loads of all parts in
-// flight together.
+// (sequence, query head): lane i reads part i's (max, sum) once, then the
+// accumulators are summed with the per-part weights, eight loads in flight.
+// The next kernel in the stream may launch at once: it waits for this grid
+// before it touches anything this kernel reads or writes.
 template <int DT>
 __global__ void __launch_bounds__(128)
 combine_sk_kernel(const SkParams sp, int grid) {
   const DecodeParams& p = sp.p;
   constexpr int PER = kD / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  allow_next_grid();
   wait_prior_grid();           // partials and the tile prefix come from the main kernel
   const int64_t row = (int64_t)blockIdx.x * 4 + warp;
   if (row >= (int64_t)p.B * p.Hq) return;
@@ -895,8 +897,15 @@ combine_sk_kernel(const SkParams sp, int grid) {
     const int slot = st >= tpb ? 0 : 1;
     return ((int64_t)cc * 2 + slot) * p.Hq + q;
   };
-  float M = -CUDART_INF_F;
-  for (int i = lane; i < nparts; i += 32) {
+  // the first 32 parts' (max, sum) stay in registers; more parts are read again
+  float M = -CUDART_INF_F, m0 = -CUDART_INF_F, l0 = 0.f;
+  const int64_t idx0 = lane < nparts ? part_index(lane) : -1;
+  if (idx0 >= 0) {
+    m0 = sp.part_m[idx0];
+    l0 = sp.part_l[idx0];
+    M = m0;
+  }
+  for (int i = lane + 32; i < nparts; i += 32) {
     const int64_t idx = part_index(i);
     if (idx >= 0) M = fmaxf(M, sp.part_m[idx]);
   }
@@ -909,7 +918,13 @@ combine_sk_kernel(const SkParams sp, int grid) {
     const int i = base + lane;
     int64_t idx = -1;
     float w = 0.f;
-    if (i < nparts) {
+    if (base == 0) {
+      idx = idx0;
+      if (idx >= 0) {
+        w = exp2f(m0 - M);
+        den = fmaf(w, l0, den);
+      }
+    } else if (i < nparts) {
       idx = part_index(i);
       if (idx >= 0) {
         w = exp2f(sp.part_m[idx] - M);
@@ -917,7 +932,7 @@ combine_sk_kernel(const SkParams sp, int grid) {
       }
     }
     const int cnt = min(32, nparts - base);
-#pragma unroll 4
+#pragma unroll 8
     for (int k = 0; k < cnt; ++k) {
       const float wk = __shfl_sync(0xFFFFFFFFu, w, k);
       const long long ik = __shfl_sync(0xFFFFFFFFu, (long long)idx, k);
