@@ -98,7 +98,7 @@ struct Tail {
   SegInfo seg[2];
   float red_buf[2][4][N];
   float alpha[2][N];
-  float lred[4][N];
+  alignas(16) float lred[4][N];
   float m_fin[N];
   int prefix[kMaxSeqs + 1];   // tiles before sequence b; prefix[B] = all tiles
   int scan[4];
@@ -346,6 +346,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     };
     int pf_b = -1, pf_len = 0;
     int32_t pf_cur = 0, pf_nxt = 0;
+    // With two Q buffers the next segment's Q is copied as soon as its buffer is
+    // free (polled once per tile, never waited on), instead of at the segment's
+    // start, one ring-depth before the MMA needs it: the copy's latency there
+    // (~4 us under load on GB300) held up the first S of every segment.
+    int next_b = -1;                   // sequence of the next segment, -1: none
+    bool q_early = false;              // the next segment's Q is already on its way
     int b = 0;
     if (t_begin < t_end) {        // the sequence holding this CTA's first tile
       int lo = 0, hi = p.B - 1;
@@ -403,7 +409,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (!ok || !sg.valid) break;
       // all query heads of the sequence (N rows; rows past Hq are never used)
       const int qb = seg_idx % Gm::kQBufs, qph = (seg_idx / Gm::kQBufs) & 1;
-      if (lane == 0) {
+      if (q_early) {
+        q_early = false;
+      } else if (lane == 0) {
         ok = mbar_wait(&tl->q_empty[qb], qph ^ 1, abort_flag, kWaitNs);
         if (ok) {
           mbar_arrive_expect_tx(&tl->q_full[qb], Gm::kQBytes);
@@ -421,9 +429,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       int kb = (sg.j0 * TT) / p.bs;
       int32_t cur = pf_cur, nxt = pf_nxt;
       const int seq_tiles = tl->prefix[sg.b + 1] - tl->prefix[sg.b];
+      next_b = -1;
       if (tl->prefix[sg.b] + sg.j1 < t_end) {   // the next segment: the next sequence with tiles
         int nb = sg.b + 1;
         while (tl->prefix[nb + 1] == tl->prefix[nb]) ++nb;
+        next_b = nb;
         pf_b = nb;
         pf_len = p.seq_lens[nb];
         pf_cur = raw_ids(nb, 0);
@@ -476,6 +486,20 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         ok = issue(&tm_k, nbox, box_tokens, tok, blk);
         if (ok && pend) ok = issue(&tm_v, pend_nbox, pend_box, pend_tok, pend_blk);
+        if (Gm::kQBufs == 2 && next_b >= 0 && !q_early) {
+          const int nqb = (seg_idx + 1) % Gm::kQBufs, nqph = ((seg_idx + 1) / Gm::kQBufs) & 1;
+          int go = 0;
+          if (lane == 0 && mbar_try_wait(&tl->q_empty[nqb], nqph ^ 1)) {
+            mbar_arrive_expect_tx(&tl->q_full[nqb], Gm::kQBytes);
+            tma_load_2d(smem + Gm::kQOff + nqb * Gm::kQBytes, &tm_q, &tl->q_full[nqb], 0,
+                        next_b * p.Hq);
+            tma_load_2d(smem + Gm::kQOff + nqb * Gm::kQBytes + N * 128, &tm_q, &tl->q_full[nqb],
+                        64, next_b * p.Hq);
+            q_issued[nqb] = nqph;
+            go = 1;
+          }
+          q_early = __shfl_sync(0xFFFFFFFFu, go, 0) != 0;
+        }
         pend = true;
         pend_nbox = nbox;
         pend_box = box_tokens;
@@ -790,11 +814,29 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       // division is the fast one (at most 2 ulp in fp32 for l in [1, 2^31], far
       // below the output's storage rounding): the IEEE one, with its slow-path
       // branch per element, cost ~2.3 us per segment on GB300.
+      // The sums are read as vectors with no per-head branch, so that the loads
+      // overlap (heads >= Hq divide by unwritten sums and are never stored); for
+      // N = 64 the registers are not there (and its batches' segments are nearly
+      // all partial).
+      if (N <= 32 && sg.direct) {
 #pragma unroll
-      for (int q = 0; q < N; ++q) {
-        if (q < Hq && sg.direct) {
-          const float l = tl->lred[0][q] + tl->lred[1][q] + tl->lred[2][q] + tl->lred[3][q];
-          acc[q] = __fdividef(acc[q], l);
+        for (int q = 0; q < N; q += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(&tl->lred[0][q]);
+          const float4 b = *reinterpret_cast<const float4*>(&tl->lred[1][q]);
+          const float4 e = *reinterpret_cast<const float4*>(&tl->lred[2][q]);
+          const float4 f = *reinterpret_cast<const float4*>(&tl->lred[3][q]);
+          acc[q] = __fdividef(acc[q], a.x + b.x + e.x + f.x);
+          acc[q + 1] = __fdividef(acc[q + 1], a.y + b.y + e.y + f.y);
+          acc[q + 2] = __fdividef(acc[q + 2], a.z + b.z + e.z + f.z);
+          acc[q + 3] = __fdividef(acc[q + 3], a.w + b.w + e.w + f.w);
+        }
+      } else if (sg.direct) {
+#pragma unroll
+        for (int q = 0; q < N; ++q) {
+          if (q < Hq) {
+            const float l = tl->lred[0][q] + tl->lred[1][q] + tl->lred[2][q] + tl->lred[3][q];
+            acc[q] = __fdividef(acc[q], l);
+          }
         }
       }
       const int64_t part0 = ((int64_t)c * 2 + sg.slot) * Hq;   // partial index of head 0
