@@ -911,15 +911,15 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
 // Merge the partials of sequences cut by CTA range boundaries.  One warp per
 // (sequence, query head): lane i reads part i's (max, sum) once, then the
 // accumulators are summed with the per-part weights, eight loads in flight.
-// The next kernel in the stream may launch at once: it waits for this grid
-// before it touches anything this kernel reads or writes.
+// No early launch of the next kernel: letting the next decode's CTAs become
+// resident while this grid runs measured 3% slower on the long-context batch
+// on GB300 (and no faster on the others).
 template <int DT>
 __global__ void __launch_bounds__(128)
 combine_sk_kernel(const SkParams sp, int grid) {
   const DecodeParams& p = sp.p;
   constexpr int PER = kD / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  allow_next_grid();
   wait_prior_grid();           // partials and the tile prefix come from the main kernel
   const int64_t row = (int64_t)blockIdx.x * 4 + warp;
   if (row >= (int64_t)p.B * p.Hq) return;
