@@ -118,6 +118,37 @@ def test_many_short_sequences(pa):
     assert_close(widen(out), scenarios.decode_f64(after), "1000 short sequences")
 
 
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (16, 2, 32), (8, 4, 8)])
+def test_empty_sequences_between_segments(pa, hq, hkv, bs):
+    """300 sequences of 0-200 tokens, every third one empty: segments follow each
+    other across empty sequences (the next segment's inputs and Q are fetched
+    ahead), finished segments stage their outputs in shared memory, and some
+    CTA ranges hold many short sequences.  Empty sequences give zero rows and
+    write nothing."""
+    g = np.random.default_rng(21)
+    lens = g.integers(1, 201, size=300)
+    lens[::3] = 0
+    w = dataclasses.replace(syn.LLAMA3_8B, name="gaps", num_seqs=300, length_kind="fixed",
+                            lens=tuple(int(x) for x in np.maximum(lens, 1)),
+                            num_q_heads=hq, num_kv_heads=hkv, block_size=bs)
+    batch = scenarios.fixed_batch(w)
+    key, value = syn.token_kv_bits(w, 300, sub=600_000)
+    seq_lens = lens.astype(np.int32)
+    live = seq_lens > 0
+    slots = _newest_slots(batch.block_tables[live], seq_lens[live], bs)
+    k_ref, v_ref = batch.k_pool.copy(), batch.v_pool.copy()
+    reshape_and_cache(k_ref, v_ref, key[live], value[live], slots)
+    dev = DeviceBatch(batch)
+    out = _fused(pa, dev, to_dev(key, w.dtype), to_dev(value, w.dtype), dev.tables,
+                 i32(seq_lens), w.scale, 200)
+    torch.cuda.synchronize()
+    _pools_equal(dev, k_ref, v_ref)
+    after = dataclasses.replace(batch, k_pool=k_ref, v_pool=v_ref, seq_lens=seq_lens)
+    got = widen(out)
+    assert not got[~live].any()
+    assert_close(got, scenarios.decode_f64(after), f"Hq={hq} Hkv={hkv} bs={bs} with gaps")
+
+
 @pytest.mark.parametrize("w", [syn.LLAMA3_8B, syn.MHA_7B, syn.LONG_CONTEXT], ids=lambda w: w.name)
 def test_benchmark_workloads(pa, w):
     """Full size, in the launch configuration the benchmark times: fused step
