@@ -25,7 +25,8 @@
 // the same number of tiles to within one, whatever the length mix.
 //
 // Roles (192 threads, one CTA per SM): warp 0 issues TMA, warp 1 issues MMA,
-// warps 2-5 run the softmax and the epilogue.  All waits are bounded.
+// warps 2-5 run the softmax and the epilogue (and, in pa_decode_append, the
+// newest tokens' cache write).  All waits are bounded.
 #include <math_constants.h>
 
 #include <mutex>
