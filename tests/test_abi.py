@@ -75,6 +75,31 @@ def test_decode_argument_checks(lib):
     assert _decode(lib, B=0) == 0                  # nothing to do, no launch
 
 
+def _decode_append(lib, **kw):
+    a = dict(out=16, q=16, k=16, v=16, key=16, value=16, tables=16, lens=16, B=2, Hq=8, Hkv=2,
+             D=128, bs=16, MB=4, NB=8, max_len=64, scale=0.1, dtype=1, pt=0, ws=256,
+             ws_bytes=1 << 20, status=None, stream=None)
+    a.update(kw)
+    return lib.pa_decode_append(a["out"], a["q"], a["k"], a["v"], a["key"], a["value"],
+                                a["tables"], a["lens"], a["B"], a["Hq"], a["Hkv"], a["D"],
+                                a["bs"], a["MB"], a["NB"], a["max_len"], a["scale"],
+                                a["dtype"], a["pt"], a["ws"], a["ws_bytes"], a["status"],
+                                a["stream"])
+
+
+def test_decode_append_argument_checks(lib):
+    """Every case returns before any launch: the step's new K/V must be given
+    and 16-byte aligned; the other checks are pa_decode's."""
+    assert _decode_append(lib, key=None) == 1
+    assert _decode_append(lib, value=None) == 1
+    assert _decode_append(lib, key=8) == 1         # misaligned
+    assert _decode_append(lib, value=24) == 1
+    assert _decode_append(lib, D=96) == 2          # head_dim not built
+    assert _decode_append(lib, Hq=6, Hkv=4) == 1
+    assert _decode_append(lib, ws_bytes=16) == 3   # workspace too small
+    assert _decode_append(lib, B=0, key=None, value=None) == 0   # nothing to do
+
+
 def test_workspace_size(lib):
     # m and l: B*Hq*P floats each; acc: B*Hq*P*D floats; 256-byte aligned parts
     n = lib.pa_decode_workspace_bytes(64, 32, 128, 4096, 0)
