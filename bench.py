@@ -1,14 +1,24 @@
 """Benchmark: one decode step of paged attention per timed step, on GB300.
 
 A step is the whole hot path over one batch: copy-on-write block copies when
-the workload shares blocks (pa_copy_blocks), the cache write of each sequence's
-newest token at the slot its block table gives (pa_append_tokens: the slot
-translation and reshape_and_cache in one launch), and decode attention over the
-paged pool (pa_decode: split-K main kernel + combine).  Inputs are synthetic and seeded; the pool is
-resident in HBM before timing starts.
+the workload shares blocks (pa_copy_blocks), then one pa_decode_append call: the
+cache write of each sequence's newest token at the slot its block table gives,
+and decode attention over the paged pool (split-K main kernel + combine).
+Inputs are synthetic and seeded; the pool is resident in HBM before timing
+starts.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Timing: after W warm-up steps, blocks of K steps run back to back between CUDA
+events (synchronize on both sides of each block), repeated at least
+--min-repeats times and for about --timed-seconds; the median block gives
+`value`.  Each decode call is then timed alone (events around it) for the
+roofline, after an L2 flush as well, and end to end with the inputs copied in
+from pinned host memory and the output copied back every step.  The default run
+(Llama-3-8B-shaped headline) also measures the long-context, shared-prefix and
+ragged decode workloads, whole-prompt prefill and a plain read stream, each in
+the `workloads` / `stream_read` objects of the same line.
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
 replica of the workload on its own GPU (the path has no cross-GPU exchange).
@@ -244,8 +254,7 @@ class NativeStep:
             self.unique_tokens = sum(prompt_lens) + len(seqs)
         else:
             lens = syn.seq_lens(w)
-            blocks = sum(-(-int(L) // bs) for L in lens)
-            nb = int(math.ceil(w.pool_factor * blocks)) + 1
+            nb = pool_blocks(w, lens)
             bm = pa.BlockManager(nb, bs, syn.shuffled_free_order(nb, syn.rng(w, "free")))
             pad = bm.allocate(1)[0]
             seqs = []
@@ -257,8 +266,6 @@ class NativeStep:
         B = len(lens)
         mb = max(bm.seq_num_blocks(s) for s in seqs)
         tables, seq_lens = bm.export(seqs, mb, pad)
-        self.pairs = (torch.tensor(pairs, dtype=torch.int32, device=dev).reshape(-1, 2)
-                      if pairs else None)
         self.lens = lens
         self.max_blocks = mb
         self.num_blocks = nb
@@ -268,20 +275,14 @@ class NativeStep:
         shape = (nb, bs, w.num_kv_heads, w.head_dim)
         self.k_pool = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(tdt)
         self.v_pool = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(tdt)
-        self.q = torch.randn((B, w.num_q_heads, w.head_dim), generator=g, device=dev).to(tdt)
-        self.key = torch.randn((B, w.num_kv_heads, w.head_dim), generator=g, device=dev).to(tdt)
-        self.value = torch.randn_like(self.key)
-        self.tables = tables.to(dev)
-        self.seq_lens = seq_lens.to(dev)
-        self.slots = torch.empty(B, dtype=torch.int32, device=dev)
-        self.out = torch.empty_like(self.q)
+        q = torch.randn((B, w.num_q_heads, w.head_dim), generator=g, device=dev).to(tdt)
+        key = torch.randn((B, w.num_kv_heads, w.head_dim), generator=g, device=dev).to(tdt)
+        value = torch.randn_like(key)
         self.max_seq_len = int(lens.max())
         self.pt = partition_tokens
-        self.ws = pa.alloc_workspace(B, w.num_q_heads, w.head_dim, self.max_seq_len,
-                                     partition_tokens, dev)
+        pa.set_decode_path(kernel)
+        self.ws = pa.workspace_for(q, self.k_pool, tables, self.max_seq_len, partition_tokens)
         P = -(-self.max_seq_len // (partition_tokens or 512))
-        # decode_slots + reshape_and_cache + decode (+ plan on the tensor-core
-        # path) + combine when a sequence spans several partitions
         self.kernel = decode_kernel_for(w, kernel)
         # append_tokens, then decode: main + combine (grouped), plan + main
         # (+ combine) (per-head), main (+ combine) (CUDA cores).  The fused step
@@ -292,198 +293,288 @@ class NativeStep:
             self.launches_per_step = 1 + 2 + (1 if P > 1 else 0)
         else:
             self.launches_per_step = 1 + 1 + (1 if P > 1 else 0)
-        if self.pairs is not None:      # copy-on-write block copies
+        if pairs:                       # copy-on-write block copies
             self.launches_per_step += 1
-        # End-to-end measurement: every step's inputs (q, the new tokens' K/V,
-        # tables, lengths, copy-on-write pairs) live packed in one pinned host
-        # buffer mirrored by one device buffer, whose views the step uses, so a
-        # step moves them with one host-to-device copy; the output comes back
-        # with one device-to-host copy.
-        parts = [("q", self.q), ("key", self.key), ("value", self.value),
-                 ("tables", self.tables), ("seq_lens", self.seq_lens)]
-        if self.pairs is not None:
-            parts.append(("pairs", self.pairs))
+        # Every step's inputs (q, the new tokens' K/V, tables, lengths,
+        # copy-on-write pairs) live packed in one pinned host buffer; two device
+        # buffers mirror it, so that the end-to-end step can copy step i+1's
+        # inputs in while step i computes.  A step moves its inputs with one
+        # host-to-device copy and its output with one device-to-host copy.
+        parts = [("q", q), ("key", key), ("value", value), ("tables", tables),
+                 ("seq_lens", seq_lens)]
+        if pairs:
+            parts.append(("pairs", torch.tensor(pairs, dtype=torch.int32).reshape(-1, 2)))
         offs, total = [], 0
         for _, t in parts:
             offs.append(total)
             total += -(-t.numel() * t.element_size() // 256) * 256
-        self.d_in = torch.empty(total, dtype=torch.uint8, device=dev)
         self.h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.bufs = []
+        for _ in range(2):
+            d_in = torch.empty(total, dtype=torch.uint8, device=dev)
+            views = {"d_in": d_in, "out": torch.empty_like(q),
+                     "h_out": torch.empty(q.shape, dtype=q.dtype).pin_memory()}
+            for (name, t), off in zip(parts, offs):
+                n = t.numel() * t.element_size()
+                dview = d_in[off:off + n].view(t.dtype).view(t.shape)
+                dview.copy_(t)
+                views[name] = dview
+            views.setdefault("pairs", None)
+            self.bufs.append(views)
         for (name, t), off in zip(parts, offs):
             n = t.numel() * t.element_size()
-            dview = self.d_in[off:off + n].view(t.dtype).view(t.shape)
-            dview.copy_(t)
             self.h_in[off:off + n].view(t.dtype).view(t.shape).copy_(t.cpu())
-            setattr(self, name, dview)
-        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.num_pairs = len(pairs)
         self.h2d_bytes = sum(t.numel() * t.element_size() for _, t in parts)
-        self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
+        self.d2h_bytes = q.numel() * q.element_size()
+        self.streams = None
 
-    def write_step(self):
-        pa = self.pa
-        if self.pairs is not None:
-            pa.pa_copy_blocks(self.k_pool, self.v_pool, self.pairs)
+    def write_step(self, s: int = 0):
+        pa, v = self.pa, self.bufs[s]
+        if v["pairs"] is not None:
+            pa.pa_copy_blocks(self.k_pool, self.v_pool, v["pairs"])
         if not self.fused:
-            pa.pa_append_tokens(self.k_pool, self.v_pool, self.key, self.value, self.tables,
-                                self.seq_lens)
+            pa.pa_append_tokens(self.k_pool, self.v_pool, v["key"], v["value"], v["tables"],
+                                v["seq_lens"])
 
-    def decode(self):
+    def decode(self, s: int = 0):
         """The decode call; with `fused`, pa_decode_append, which also writes the
         step's new tokens (inside the grouped kernel, else as a launch before it)."""
+        v = self.bufs[s]
         if self.fused:
-            self.pa.pa_decode_append(self.out, self.q, self.k_pool, self.v_pool, self.key,
-                                     self.value, self.tables, self.seq_lens, self.w.scale,
+            self.pa.pa_decode_append(v["out"], v["q"], self.k_pool, self.v_pool, v["key"],
+                                     v["value"], v["tables"], v["seq_lens"], self.w.scale,
                                      max_seq_len=self.max_seq_len, partition_tokens=self.pt,
                                      workspace=self.ws)
         else:
-            self.pa.pa_decode(self.out, self.q, self.k_pool, self.v_pool, self.tables,
-                              self.seq_lens, self.w.scale, max_seq_len=self.max_seq_len,
+            self.pa.pa_decode(v["out"], v["q"], self.k_pool, self.v_pool, v["tables"],
+                              v["seq_lens"], self.w.scale, max_seq_len=self.max_seq_len,
                               partition_tokens=self.pt, workspace=self.ws)
 
-    def run(self):
-        self.write_step()
-        self.decode()
+    def run(self, s: int = 0):
+        self.write_step(s)
+        self.decode(s)
 
-    def run_e2e(self):
-        # the step's inputs from pinned host memory (one copy), the result back
-        self.d_in.copy_(self.h_in, non_blocking=True)
-        self.run()
-        self.h_out.copy_(self.out, non_blocking=True)
+    def run_e2e_serial(self):
+        """One step with its copies in line: inputs in, the step, the output back."""
+        v = self.bufs[0]
+        v["d_in"].copy_(self.h_in, non_blocking=True)
+        self.run(0)
+        v["h_out"].copy_(v["out"], non_blocking=True)
+
+    def e2e_block(self, K: int, start_event):
+        """K end-to-end steps with the copies pipelined: step i+1's inputs are
+        copied in (its own stream) while step i computes, and step i's output is
+        copied back (a third stream) while step i+1 computes.  Two device buffer
+        sets alternate; events order every reuse.  Every step still moves its
+        whole input in and its whole output out; the block ends when the last
+        output is in host memory."""
+        torch = self.torch
+        if self.streams is None:
+            self.streams = (torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev))
+            E = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+            self.ev_ready, self.ev_computed, self.ev_drained = E(), E(), E()
+        h2d, d2h = self.streams
+        main = torch.cuda.current_stream()
+
+        def copy_in(i):
+            s = i % 2
+            h2d.wait_event(start_event)
+            if i >= 2:          # step i-2 has finished reading buffer s
+                h2d.wait_event(self.ev_computed[s])
+            with torch.cuda.stream(h2d):
+                self.bufs[s]["d_in"].copy_(self.h_in, non_blocking=True)
+            self.ev_ready[s].record(h2d)
+
+        copy_in(0)
+        for i in range(K):
+            s = i % 2
+            if i + 1 < K:
+                copy_in(i + 1)
+            main.wait_event(self.ev_ready[s])
+            if i >= 2:          # step i-2's output has left buffer s
+                main.wait_event(self.ev_drained[s])
+            self.run(s)
+            self.ev_computed[s].record(main)
+            d2h.wait_event(self.ev_computed[s])
+            with torch.cuda.stream(d2h):
+                self.bufs[s]["h_out"].copy_(self.bufs[s]["out"], non_blocking=True)
+            self.ev_drained[s].record(d2h)
+        for s in range(min(K, 2)):
+            main.wait_event(self.ev_drained[s])
 
 
-def run_native(args, dist_info):
+def pool_blocks(w, lens) -> int:
+    """Physical blocks of a fixed-batch workload's pool: 1.25 x the blocks the
+    batch needs, plus the padding block table entries past a sequence point at."""
+    need = sum(-(-int(L) // w.block_size) for L in lens)
+    return int(math.ceil(w.pool_factor * need)) + 1
+
+
+def workload_config(w, lens, num_blocks, args) -> dict:
+    """The `config` object of a decode line; both arms emit the same one."""
+    kvb = kv_bytes(lens, w)
+    return {
+        "workload": w.name, "num_seqs": int(len(lens)), "num_q_heads": w.num_q_heads,
+        "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+        "block_size": w.block_size, "seq_lens": {
+            "fixed": list(w.lens), "uniform": f"uniform [{w.lo},{w.hi}]",
+            "lognormal": f"lognormal median {w.median:g} sigma {w.sigma:g} clipped [{w.lo},{w.hi}]",
+            "shared_prefix": f"{w.num_prompts} prompts x {w.samples_per_prompt} samples, "
+                             f"prefix {w.prefix_tokens}+U{{0..{w.prefix_jitter}}}, +1 token"}[w.length_kind],
+        "total_tokens": int(np.sum(lens)), "num_blocks": int(num_blocks),
+        "partition_tokens": args.partition_tokens or 512,
+        "kv_bytes_per_step": kvb,
+        "l2": f"inputs larger than L2: {kvb / 2**20:.0f} MiB of K/V read per step vs "
+              f"{L2_BYTES / 2**20:.0f} MiB L2; no flush between steps (the l2_flushed "
+              f"figure flushes before each call)",
+        "parallelism": f"replicas x{args.world}" if args.world > 1 else "1 GPU",
+    }
+
+
+def agree_max(n: int, world: int, device) -> int:
+    """The largest of the ranks' values of n (every rank runs the same loop)."""
+    if world <= 1:
+        return n
     import torch
-    import paged_kv_cache_301_gb300 as pa
-    from paged_kv_cache_301_gb300 import build as _build
+    t = torch.tensor([n], dtype=torch.int64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return int(t.item())
 
-    rank, world, local = dist_info
-    _build.build()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    w = workload(args.workload, args.block_size)
-    cpu_baseline = None
-    if rank == 0 and not args.no_cpu_baseline and w.length_kind != "shared_prefix":
-        # before the first GPU call: the oracle's pool is a spawn pool anyway
-        cpu_baseline = cpu_oracle_baseline(w, budget_s=args.cpu_budget)
-    pa.set_decode_path(args.kernel)
-    step = NativeStep(pa, torch, w, dev, args.partition_tokens, args.kernel,
-                      fused=not args.split_step)
+
+def barrier(world):
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+
+
+def repeat_count(block_ms: float, args) -> int:
+    """Repeats of the K-step block: at least --min-repeats, and enough for about
+    --timed-seconds of timed work (so the clock sampler sees the load)."""
+    want = int(math.ceil(args.timed_seconds * 1e3 / max(block_ms, 1e-3)))
+    return max(args.min_repeats, min(want, args.max_repeats))
+
+
+def measure_decode(torch, step, args, world, dev, flushed: bool):
+    """Time one workload's decode step.  Returns per-repeat figures (max over
+    ranks): ms per step of each K-step block run back to back, ms of each decode
+    call with events around it, ms of calls after an L2 flush, and ms per step of
+    end-to-end blocks (pipelined and serial copies)."""
+    K = args.steps
     stream = torch.cuda.current_stream()
-
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    def block(fn):
+        torch.cuda.synchronize()
+        barrier(world)
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    reps = agree_max(repeat_count(block(step.run), args), world, dev)
     clocks = ClockSampler(gpu_uuid(torch, dev))
     clocks.start()
     time.sleep(0.25)           # let the sampler take its first reading
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
-    # the K steps back to back (events between the steps would break the
-    # programmatic-dependent-launch chain from one step's last kernel to the
+    # the K steps of a block back to back (events between the steps would break
+    # the programmatic-dependent-launch chain from one step's last kernel to the
     # next step's first)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step.run()
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    step_ms = [block(step.run) / K for _ in range(reps)]
     wall = time.perf_counter() - wall0
-    # then K more with events around each decode call, for its own duration
-    for i in range(args.steps):
-        step.write_step()
-        ev[i][0].record(stream)
-        step.decode()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    # then each decode call with events around it, for its own duration
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    call_ms = []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        barrier(world)
+        for i in range(K):
+            step.write_step()
+            ev[i][0].record(stream)
+            step.decode()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        call_ms += [x.elapsed_time(y) for x, y in ev]
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    decode_ms = [a.elapsed_time(b) for a, b in ev]
-
+    flushed_ms = []
+    if flushed:
+        # L2 flush before each call: write one buffer of twice the L2, then read
+        # another, so that the L2 holds clean lines of neither the workload nor
+        # the first buffer (dirty lines would be written back inside the call)
+        fw = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        fr = torch.zeros(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        for _ in range(max(args.min_repeats, 25)):
+            step.write_step()
+            fw.zero_()
+            fr.sum()
+            a.record(stream)
+            step.decode()
+            b.record(stream)
+            torch.cuda.synchronize()
+            flushed_ms.append(a.elapsed_time(b))
+        del fw, fr
     # end to end: host buffers in, host result out, every step
-    for _ in range(max(3, args.warmup // 4)):
-        step.run_e2e()
+    for _ in range(3):
+        step.run_e2e_serial()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step.run_e2e()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms, e2e_serial_ms = [], []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        barrier(world)
+        a.record(stream)
+        step.e2e_block(K, a)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(a.elapsed_time(b) / K)
+    for _ in range(reps):
+        e2e_serial_ms.append(block(step.run_e2e_serial) / K)
+    out = {"reps": reps, "step_ms": step_ms, "call_ms": call_ms, "flushed_ms": flushed_ms,
+           "e2e_ms": e2e_ms, "e2e_serial_ms": e2e_serial_ms, "clocks": clk, "wall_s": wall}
+    for key in ("step_ms", "call_ms", "flushed_ms", "e2e_ms", "e2e_serial_ms"):
+        if out[key]:
+            out[key] = slowest_rank(out[key], world, dev)
+    return out
 
-    total_ms, e2e_ms = slowest_rank([total_ms, e2e_ms], world, dev)
-    if rank != 0:
-        return None
 
-    ms_step = total_ms / args.steps
-    kvb = kv_bytes(step.lens, w)
+def med(xs):
+    return statistics.median(xs) if xs else None
+
+
+def decode_entry(step, m, w, world, peak, peak_kind, args) -> dict:
+    """Figures of one decode workload from its measurements."""
+    K = args.steps
     B = len(step.lens)
-    value = whole_job_gbs(kvb, world, ms_step)
-    dec_avg_ms = sum(decode_ms) / len(decode_ms)
+    kvb = kv_bytes(step.lens, w)
+    ms_step = med(m["step_ms"])
+    call = med(m["call_ms"])
     dec_bytes = decode_bytes(step.lens, w, step.max_blocks)
     if step.fused:     # the new tokens' K/V read once and written to the pool
         dec_bytes += 4 * B * w.num_kv_heads * w.head_dim * w.elem_bytes
-    peak, peak_kind = measured_peaks()
-    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(w.name, step.kernel)
-    result = {
-        "metric": METRIC,
-        "value": round(value, 1),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
+    achieved = dec_bytes / (call * 1e-3) / 1e9
+    gbs = lambda ms: round(whole_job_gbs(kvb, world, ms), 1)
+    e = {
+        "value": gbs(ms_step), "unit": "GB/s",
         "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": syn.DTYPE_NAMES[w.dtype],
-        "data": "synthetic (seeded N(0,1) q/K/V; block ids a seeded permutation)",
-        "config": {
-            "workload": w.name, "num_seqs": B, "num_q_heads": w.num_q_heads,
-            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-            "block_size": w.block_size, "seq_lens": {
-                "fixed": list(w.lens), "uniform": f"uniform [{w.lo},{w.hi}]",
-                "lognormal": f"lognormal median {w.median:g} sigma {w.sigma:g} clipped [{w.lo},{w.hi}]",
-                "shared_prefix": f"{w.num_prompts} prompts x {w.samples_per_prompt} samples, "
-                                 f"prefix {w.prefix_tokens}+U{{0..{w.prefix_jitter}}}, +1 token"}[w.length_kind],
-            "total_tokens": int(np.sum(step.lens)), "num_blocks": step.num_blocks,
-            "partition_tokens": args.partition_tokens or 512,
-            "kv_bytes_per_step": kvb,
-            "l2": f"inputs larger than L2: {kvb / 2**20:.0f} MiB of K/V read per step vs "
-                  f"{L2_BYTES / 2**20:.0f} MiB L2; no flush",
-            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-            "decode_kernel": {"tcg": "tcgen05 + TMA, whole-block (decode_tcg_kernel)",
-                              "tc_head": "tcgen05 + TMA, per KV head (decode_tc_kernel)",
-                              "simt": "CUDA cores (decode_simt_kernel)"}[step.kernel],
-            "step": ("pa_decode_append: new tokens' cache write + decode in one call"
-                     if step.fused else "pa_append_tokens, then pa_decode"),
-        },
+        "ms_per_step_mean": round(statistics.fmean(m["step_ms"]), 5),
+        "repeats": m["reps"], "steps_per_repeat": K,
         "tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
-        "unique_kv_gbs": round(whole_job_gbs(step.unique_tokens * w.num_kv_heads * w.head_dim * 4,
-                                             world, ms_step), 1),
-        "cow_block_copies_per_step": 0 if step.pairs is None else int(step.pairs.shape[0]),
-        "kv_frac_of_peak": round(value / world / peak, 4),
-        "wall_s": round(wall, 4),
-        "e2e": {
-            "value": round(world * kvb / (e2e_ms / args.steps * 1e-3) / 1e9, 1),
-            "unit": "GB/s",
-            "ms_per_step": round(e2e_ms / args.steps, 5),
-            "h2d_bytes_per_step": step.h2d_bytes,
-            "d2h_bytes_per_step": step.d2h_bytes,
-        },
-        "gpu_launches": step.launches_per_step * args.steps,
+        "kv_frac_of_peak": round(whole_job_gbs(kvb, 1, ms_step) / peak, 4),
+        "config": workload_config(w, step.lens, step.num_blocks, args),
+        "decode_kernel": {"tcg": "tcgen05 + TMA, whole-block (decode_tcg_kernel)",
+                          "tc_head": "tcgen05 + TMA, per KV head (decode_tc_kernel)",
+                          "simt": "CUDA cores (decode_simt_kernel)"}[step.kernel],
+        "step": ("pa_decode_append: new tokens' cache write + decode in one call"
+                 if step.fused else "pa_append_tokens, then pa_decode")
+                + (f"; pa_copy_blocks of {step.num_pairs} copy-on-write pairs first"
+                   if step.num_pairs else ""),
+        "gpu_launches_per_step": step.launches_per_step,
         "roofline": {
             "kernel": ("pa_decode_append" if step.fused else "pa_decode") + " " +
                       {"tcg": "(stream-K main + combine)" + (
@@ -498,14 +589,251 @@ def run_native(args, dist_info):
             "peak_kind": peak_kind,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic,
+            "traffic": recorded_traffic(w.name, step.kernel),
             "traffic_unit": "bytes per decode_tcg_kernel launch (ncu dram read + write)",
             "algorithmic_bytes": dec_bytes,
-            "avg_launch_ms": round(dec_avg_ms, 5),
+            "avg_launch_ms": round(call, 5),
+            "launch_ms_mean": round(statistics.fmean(m["call_ms"]), 5),
+            "launch_timing": f"median of {len(m['call_ms'])} decode calls, CUDA events around "
+                             f"each call on the launching stream",
         },
-        "clocks": clk,
-        "cpu_baseline": cpu_baseline,
+        "e2e": {
+            "value": gbs(med(m["e2e_ms"])), "unit": "GB/s",
+            "ms_per_step": round(med(m["e2e_ms"]), 5),
+            "h2d_bytes_per_step": step.h2d_bytes,
+            "d2h_bytes_per_step": step.d2h_bytes,
+            "copies": "pinned host inputs in and the output back every step; step i+1's "
+                      "input copy and step i-1's output copy overlap step i (two device "
+                      "buffer sets)",
+            "serial": {"value": gbs(med(m["e2e_serial_ms"])),
+                       "ms_per_step": round(med(m["e2e_serial_ms"]), 5),
+                       "copies": "in, step, out, in line on one stream"},
+        },
+        "clocks": m["clocks"],
+        "wall_s": round(m["wall_s"], 4),
     }
+    if w.length_kind == "shared_prefix":
+        e["unique_kv_gbs"] = round(whole_job_gbs(step.unique_tokens * w.num_kv_heads *
+                                                 w.head_dim * 4, world, ms_step), 1)
+        e["cow_block_copies_per_step"] = step.num_pairs
+        e["roofline"]["note"] = ("logical bytes: the samples of a prompt read its shared "
+                                 "prefix blocks, which stay in L2 between them; "
+                                 "unique_kv_gbs counts each physical token once")
+    if m["flushed_ms"]:
+        fl = med(m["flushed_ms"])
+        e["l2_flushed"] = {"avg_launch_ms": round(fl, 5),
+                           "achieved": round(dec_bytes / (fl * 1e-3) / 1e9, 1),
+                           "frac": round(dec_bytes / (fl * 1e-3) / 1e9 / peak, 4),
+                           "calls": len(m["flushed_ms"]),
+                           "how": "before each call: write a 2x L2 buffer, then read "
+                                  "another; median of the calls"}
+        e["warm"] = {"avg_launch_ms": e["roofline"]["avg_launch_ms"],
+                     "achieved": e["roofline"]["achieved"],
+                     "how": "calls back to back (the previous call's data may sit in L2)"}
+    return e
+
+
+class PrefillStep:
+    """Device state of one prefill workload: every token's K/V in a pool reached
+    through block tables (the library's block manager over a shuffled free
+    stack), queries for the last n_b tokens of each sequence."""
+
+    def __init__(self, pa, torch, w, dev):
+        self.pa, self.torch, self.w = pa, torch, w
+        lens = syn.seq_lens(w)
+        qn = syn.query_counts(w, lens)
+        bs = w.block_size
+        nb = pool_blocks(w, lens)
+        bm = pa.BlockManager(nb, bs, syn.shuffled_free_order(nb, syn.rng(w, "free")))
+        pad = bm.allocate(1)[0]
+        seqs = [bm.new_sequence(int(L)) for L in lens]
+        mb = max(bm.seq_num_blocks(s) for s in seqs)
+        tables, seq_lens = bm.export(seqs, mb, pad)
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed)
+        tdt = torch.bfloat16 if w.dtype == syn.BFLOAT16 else torch.float16
+        shape = (nb, bs, w.num_kv_heads, w.head_dim)
+        self.k_pool = torch.randn(shape, generator=g, device=dev).to(tdt)
+        self.v_pool = torch.randn(shape, generator=g, device=dev).to(tdt)
+        q_start = np.concatenate([[0], np.cumsum(qn)]).astype(np.int32)
+        self.total_q = int(q_start[-1])
+        self.q = torch.randn((self.total_q, w.num_q_heads, w.head_dim), generator=g,
+                             device=dev).to(tdt)
+        self.out = torch.empty_like(self.q)
+        self.tables = tables.to(dev)
+        self.seq_lens = seq_lens.to(dev)
+        self.q_start = torch.from_numpy(q_start).to(dev)
+        self.max_q = int(qn.max())
+        self.lens, self.qn = lens, qn
+        # causal (query, key) pairs per head: query i of n attends to L - n + i + 1 keys
+        self.pairs = int(sum(int(n) * (int(L) - int(n)) + int(n) * (int(n) + 1) // 2
+                             for L, n in zip(lens, qn)))
+
+    def run(self):
+        self.pa.pa_prefill(self.out, self.q, self.k_pool, self.v_pool, self.tables,
+                           self.seq_lens, self.q_start, self.w.scale, max_q_len=self.max_q)
+
+
+def tensor_peak():
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    if "bf16_tflops" in peaks:
+        return float(peaks["bf16_tflops"]), "measured (cuBLAS bf16, burst)"
+    return 1900.0, "fallback"
+
+
+def measure_prefill(torch, pa, name, args, dev, kernel="auto") -> dict:
+    """Prefill TFLOP/s on one workload: median over repeats of K back-to-back calls."""
+    w = syn.WORKLOADS[name]
+    pa.set_prefill_path("simt" if kernel == "simt" else "auto")
+    ps = PrefillStep(pa, torch, w, dev)
+    stream = torch.cuda.current_stream()
+    K = args.steps
+    for _ in range(args.warmup):
+        ps.run()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def block():
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(K):
+            ps.run()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K
+
+    reps = repeat_count(block() * K, args)
+    clocks = ClockSampler(gpu_uuid(torch, dev))
+    clocks.start()
+    time.sleep(0.25)
+    ms_list = [block() for _ in range(reps)]
+    clk = clocks.stop()
+    ms = med(ms_list)
+    flops = 4.0 * w.head_dim * w.num_q_heads * ps.pairs     # q.k and p.v per pair and head
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak, peak_kind = tensor_peak()
+    res = {
+        "value": round(tflops, 1), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+        "ms_per_step_mean": round(statistics.fmean(ms_list), 5), "repeats": reps,
+        "steps_per_repeat": K,
+        "config": {"workload": name, "num_seqs": len(ps.lens), "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "total_tokens": int(np.sum(ps.lens)),
+                   "query_tokens": ps.total_q, "causal_pairs_per_head": ps.pairs},
+        "tokens_per_s": round(ps.total_q / (ms * 1e-3), 1),
+        "roofline": {"kernel": "prefill_simt_kernel" if kernel == "simt" else "prefill_tc_kernel",
+                     "bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                     "algorithmic_flops": flops, "avg_launch_ms": round(ms, 5)},
+        "clocks": clk, "gpu_launches_per_step": 1,
+    }
+    pa.set_prefill_path("auto")
+    return res
+
+
+def measure_stream_read(torch, pa, dev, args) -> dict:
+    """The library's plain read stream over a 4 GiB buffer (context for the
+    decode kernels' bandwidth): median of repeated passes."""
+    nbytes = 4 << 30
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    buf.random_(0, 256)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        pa.pa_stream_read(buf)
+    ms = []
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(max(args.min_repeats, 25)):
+        a.record(stream)
+        pa.pa_stream_read(buf)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    del buf
+    m = med(ms)
+    return {"gbs": round(nbytes / (m * 1e-3) / 1e9, 1), "bytes": nbytes, "passes": len(ms),
+            "ms": round(m, 5), "kernel": "stream_read_kernel (pa_stream_read): contiguous "
+            "16-byte loads, 8 in flight per thread, 4 x 512 threads per SM",
+            "what": "read-only HBM bandwidth reached without a gather, same run; the "
+                    "roofline peak is the copy (read + write) figure"}
+
+
+# Workloads measured beside the headline one in a default run.
+EXTRA_WORKLOADS = ("long_context", "shared_prefix", "ragged")
+
+
+def run_native(args, dist_info):
+    import torch
+    import paged_kv_cache_301_gb300 as pa
+    from paged_kv_cache_301_gb300 import build as _build
+
+    rank, world, local = dist_info
+    args.world = world
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workload(args.workload, args.block_size)
+    cpu_baseline = None
+    if rank == 0 and not args.no_cpu_baseline and w.length_kind != "shared_prefix":
+        # before the first GPU call: the oracle's pool is a spawn pool anyway
+        cpu_baseline = cpu_oracle_baseline(w, budget_s=args.cpu_budget)
+    peak, peak_kind = measured_peaks()
+    pa.set_decode_path(args.kernel)
+    step = NativeStep(pa, torch, w, dev, args.partition_tokens, args.kernel,
+                      fused=not args.split_step)
+    m = measure_decode(torch, step, args, world, dev, flushed=True)
+    head = decode_entry(step, m, w, world, peak, peak_kind, args)
+    del step
+    torch.cuda.empty_cache()
+    workloads = {}
+    stream_read = None
+    if args.workload == "llama3_8b" and not args.single_workload:
+        for name in EXTRA_WORKLOADS:
+            wx = workload(name, None)
+            st = NativeStep(pa, torch, wx, dev, args.partition_tokens, args.kernel,
+                            fused=not args.split_step)
+            workloads[name] = decode_entry(st, measure_decode(torch, st, args, world, dev,
+                                                              flushed=False),
+                                           wx, world, peak, peak_kind, args)
+            del st
+            torch.cuda.empty_cache()
+        if args.kernel in ("auto", "tc"):
+            workloads["prefill"] = measure_prefill(torch, pa, "prefill", args, dev)
+            torch.cuda.empty_cache()
+        stream_read = measure_stream_read(torch, pa, dev, args)
+    if rank != 0:
+        return None
+    reps = head["repeats"]
+    result = {
+        "metric": METRIC,
+        "value": head["value"],
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": syn.DTYPE_NAMES[w.dtype],
+        "data": "synthetic (seeded N(0,1) q/K/V; block ids a seeded permutation)",
+        "config": head.pop("config"),
+        "timing": (f"value and ms_per_step: median over {reps} repeats of the K = {args.steps} "
+                   f"steps timed back to back between CUDA events (synchronize on both "
+                   f"sides of each repeat; ms_per_step_mean is the mean)"),
+    }
+    result.update(head)
+    result["gpu_launches"] = head["gpu_launches_per_step"] * args.steps * reps
+    result["cpu_baseline"] = cpu_baseline
+    if workloads:
+        result["workloads"] = workloads
+    if stream_read is not None:
+        result["stream_read"] = stream_read
+        result["roofline"]["frac_of_stream_read"] = round(
+            result["roofline"]["achieved"] / stream_read["gbs"], 4)
     return result
 
 
@@ -605,6 +933,31 @@ def run_blocks(args):
     }
 
 
+def prefill_cpu_baseline(name: str) -> dict:
+    """The fp64 oracle on 16 sampled query rows (all heads) of a prefill
+    workload, one host thread, on the oracle's own copy of the inputs."""
+    from oracle import scenarios
+    w = syn.WORKLOADS[name]
+    pb = scenarios.prefill_batch(w, fill_all=True)
+    b = pb.batch
+    total_q = int(pb.q_start[-1])
+    g = np.random.default_rng(3)
+    rows = sorted(set(int(x) for x in g.integers(0, total_q, size=16)))
+    t0 = time.perf_counter()
+    scenarios.prefill_f64(pb, rows=rows)
+    el = time.perf_counter() - t0
+    # flops of the sampled rows: each row sees position + 1 keys, all heads
+    pos = []
+    for r in rows:
+        s_ = int(np.searchsorted(pb.q_start, r, side="right")) - 1
+        n_ = int(pb.q_start[s_ + 1] - pb.q_start[s_])
+        pos.append(int(b.seq_lens[s_]) - n_ + (r - int(pb.q_start[s_])))
+    f_rows = 4.0 * w.head_dim * w.num_q_heads * sum(p_ + 1 for p_ in pos)
+    return {"value": round(f_rows / el / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+            "kind": "oracle", "sample": f"{len(rows)} query rows (all heads) of the {name} "
+                                        f"workload, fp64 oracle, {el:.1f} s"}
+
+
 def run_prefill(args):
     """--op prefill: causal multi-query attention over the paged pool (pa_prefill)
     on the whole-prompt or the chunked-prefill workload; FLOP/s of the causal
@@ -612,93 +965,25 @@ def run_prefill(args):
     import torch
     import paged_kv_cache_301_gb300 as pa
     from paged_kv_cache_301_gb300 import build as _build
-    from oracle import scenarios
-    from oracle.prefill import causal_pairs
 
     _build.build()
     name = args.workload if args.workload in ("prefill", "chunked_prefill") else "prefill"
     w = syn.WORKLOADS[name]
-    pb = scenarios.prefill_batch(w, fill_all=True)
-    b = pb.batch
+    cpu = None if args.no_cpu_baseline else prefill_cpu_baseline(name)
     torch.cuda.set_device(0)
-    dt = {syn.FLOAT16: torch.float16, syn.BFLOAT16: torch.bfloat16}[w.dtype]
-
-    def dev(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(dt)
-
-    pa.set_prefill_path("simt" if args.kernel == "simt" else "auto")
-    kp, vp, q = dev(b.k_pool), dev(b.v_pool), dev(pb.q)
-    tables = torch.from_numpy(b.block_tables).cuda()
-    lens = torch.from_numpy(b.seq_lens).cuda()
-    qst = torch.from_numpy(pb.q_start).cuda()
-    out = torch.empty_like(q)
-    max_q = int(np.diff(pb.q_start).max())
-    stream = torch.cuda.current_stream()
-
-    def step():
-        pa.pa_prefill(out, q, kp, vp, tables, lens, qst, w.scale, max_q_len=max_q)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(gpu_uuid(torch, torch.device("cuda", 0)))
-    clocks.start()
-    time.sleep(0.25)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    pairs = causal_pairs(b.seq_lens, pb.q_start)
-    flops = 4.0 * w.head_dim * w.num_q_heads * pairs          # q.k and p.v per pair and head
-    tflops = flops / (ms * 1e-3) / 1e12
-    total_q = int(pb.q_start[-1])
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except (OSError, ValueError):
-        pass
-    peak = peaks.get("bf16_tflops") or 1900.0
-    peak_kind = "measured (cuBLAS bf16, burst)" if "bf16_tflops" in peaks else "fallback"
-    cpu = None
-    if not args.no_cpu_baseline:
-        g = np.random.default_rng(3)
-        rows = sorted(set(int(x) for x in g.integers(0, total_q, size=16)))
-        t0 = time.perf_counter()
-        scenarios.prefill_f64(pb, rows=rows)
-        el = time.perf_counter() - t0
-        # flops of the sampled rows: each row sees position + 1 keys, all heads
-        pos = []
-        for r in rows:
-            s_ = int(np.searchsorted(pb.q_start, r, side="right")) - 1
-            n_ = int(pb.q_start[s_ + 1] - pb.q_start[s_])
-            pos.append(int(b.seq_lens[s_]) - n_ + (r - int(pb.q_start[s_])))
-        f_rows = 4.0 * w.head_dim * w.num_q_heads * sum(p_ + 1 for p_ in pos)
-        cpu = {"value": round(f_rows / el / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
-               "kind": "oracle", "sample": f"{len(rows)} query rows (all heads) of the {name} "
-                                           f"workload, fp64 oracle, {el:.1f} s"}
-    return {
+    r = measure_prefill(torch, pa, name, args, torch.device("cuda", 0),
+                        kernel="simt" if args.kernel == "simt" else "auto")
+    out = {
         "metric": "paged prefill attention TFLOP/s (causal pairs x 4 x head_dim x heads)",
-        "value": round(tflops, 1), "unit": "TFLOP/s", "op": "prefill", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "value": r["value"], "unit": "TFLOP/s", "op": "prefill", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
         "higher_is_better": True, "dtype": syn.DTYPE_NAMES[w.dtype],
         "data": "synthetic (seeded N(0,1) q/K/V; block ids a seeded permutation)",
-        "config": {"workload": name, "num_seqs": len(b.seq_lens), "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "block_size": w.block_size, "total_tokens": int(b.seq_lens.sum()),
-                   "query_tokens": total_q, "causal_pairs_per_head": pairs},
-        "tokens_per_s": round(total_q / (ms * 1e-3), 1),
-        "roofline": {"kernel": "prefill_simt_kernel" if args.kernel == "simt" else "prefill_tc_kernel",
-                     "bound": "tensor",
-                     "achieved": round(tflops, 1), "peak": peak, "peak_kind": peak_kind,
-                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                     "algorithmic_flops": flops, "avg_launch_ms": round(ms, 5)},
-        "clocks": clk, "cpu_baseline": cpu, "gpu_launches": args.steps,
     }
+    out.update(r)
+    out["cpu_baseline"] = cpu
+    out["gpu_launches"] = args.steps * r["repeats"]
+    return out
 
 
 def run_allocsim(args):
@@ -785,6 +1070,20 @@ def _pool_task(args):
     return float(out[b].sum())
 
 
+def _pool_task_timed(args):
+    """Run the units (b, heads) `repeats` times in this worker; the seconds are
+    measured here, so no inter-process traffic is counted."""
+    units, scale, dtype, repeats = args
+    from oracle.attention import paged_decode_attention
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        for b, heads in units:
+            paged_decode_attention(_shared["q"][1], _shared["k"][1], _shared["v"][1],
+                                   _shared["tables"][1], _shared["lens"][1], scale,
+                                   sequences=[b], heads=heads, dtype=dtype)
+    return time.perf_counter() - t0
+
+
 class OraclePool:
     """The fp64 oracle over a host copy of the workload, run on a spawn pool with
     one single-threaded worker per host core."""
@@ -821,6 +1120,12 @@ class OraclePool:
                                    for b, heads in units], chunksize=1)
         return time.perf_counter() - t0
 
+    def run_single(self, units, repeats=1):
+        """One worker (one host thread) runs the units `repeats` times in turn;
+        returns its seconds."""
+        return self.pool.apply(_pool_task_timed,
+                               ((units, self.batch.scale, self.batch.dtype, repeats),))
+
     def unit_bytes(self, units):
         w = self.w
         G = w.group
@@ -836,9 +1141,32 @@ class OraclePool:
             s.unlink()
 
 
+def single_thread_baseline(op, units_all, budget_s: float) -> dict:
+    """The oracle on one host thread: whole (sequence, all heads) units in turn,
+    as many as fit about budget_s (at least one), repeated for short workloads."""
+    w = op.w
+    t1 = op.run_single(units_all[:1])
+    n = max(1, min(len(units_all), int(budget_s / max(t1, 1e-6))))
+    units = units_all[:n]
+    repeats = 1
+    if n == len(units_all):
+        t_all = op.run_single(units)
+        repeats = max(1, int(budget_s / max(t_all, 1e-6)))
+    secs = op.run_single(units, repeats)
+    lens = op.batch.seq_lens
+    kvb = repeats * sum(int(lens[b]) for b, _ in units) * w.num_kv_heads * w.head_dim * 2 * \
+        w.elem_bytes
+    return {"workload": w.name, "value": round(kvb / secs / 1e9, 5), "unit": "GB/s",
+            "cores": 1, "tokens_per_s": round(repeats * len(units) / secs, 3),
+            "sample": f"{len(units)} of {len(units_all)} sequences (all {w.num_q_heads} query "
+                      f"heads) x {repeats} pass(es), {secs:.2f} s on one single-threaded "
+                      f"worker process"}
+
+
 def cpu_oracle_baseline(w, budget_s=15.0):
     """Oracle throughput on the host cores: whole passes over the batch until
-    about budget_s of CPU work (wall time x worker processes) is spent."""
+    about budget_s of CPU work (wall time x worker processes) is spent; then the
+    same oracle on one host thread, on this workload and on the tiny one."""
     op = OraclePool(w)
     try:
         B = len(op.batch.seq_lens)
@@ -849,18 +1177,30 @@ def cpu_oracle_baseline(w, budget_s=15.0):
             secs += op.run(units)
             passes += 1
         kvb = passes * kv_bytes(op.batch.seq_lens, w)
-        return {"value": round(kvb / secs / 1e9, 4), "unit": "GB/s", "cores": op.cores,
-                "kind": "oracle",
-                "sample": f"fp64 oracle, {passes} full pass(es) over the {B} sequences x "
-                          f"{w.num_q_heads} query heads of the {w.name} workload, {secs:.2f} s "
-                          f"wall on {op.cores} single-threaded worker processes",
-                "tokens_per_s": round(passes * B / secs, 3)}
+        res = {"value": round(kvb / secs / 1e9, 4), "unit": "GB/s", "cores": op.cores,
+               "kind": "oracle",
+               "sample": f"fp64 oracle, {passes} full pass(es) over the {B} sequences x "
+                         f"{w.num_q_heads} query heads of the {w.name} workload, {secs:.2f} s "
+                         f"wall on {op.cores} single-threaded worker processes",
+               "tokens_per_s": round(passes * B / secs, 3)}
+        single = [single_thread_baseline(op, units, budget_s / 5)]
     finally:
         op.close()
+    if w.name != "tiny":
+        tiny = syn.WORKLOADS["tiny"]
+        op = OraclePool(tiny, cores=1)
+        try:
+            tu = [(b, list(range(tiny.num_q_heads))) for b in range(len(op.batch.seq_lens))]
+            single.append(single_thread_baseline(op, tu, budget_s / 15))
+        finally:
+            op.close()
+    res["single_thread"] = single
+    return res
 
 
 def run_reference(args, dist_info):
     rank, world, _ = dist_info
+    args.world = world
     if rank != 0:
         return None
     w = workload(args.workload, args.block_size)
@@ -892,9 +1232,8 @@ def run_reference(args, dist_info):
             "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) q/K/V; block ids a seeded permutation)",
-            "config": {"workload": w.name, "num_seqs": B, "num_q_heads": w.num_q_heads,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                       "block_size": w.block_size},
+            "config": workload_config(w, op.batch.seq_lens, pool_blocks(w, op.batch.seq_lens),
+                                      args),
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": op.cores,
                              "kind": "oracle",
@@ -924,8 +1263,16 @@ def dist_setup(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--min-repeats", type=int, default=25,
+                    help="repeats of the K-step timed block at least (the median is reported)")
+    ap.add_argument("--max-repeats", type=int, default=1000)
+    ap.add_argument("--timed-seconds", type=float, default=0.6,
+                    help="aim for about this much timed work per loop and workload")
+    ap.add_argument("--single-workload", action="store_true",
+                    help="measure only --workload (the default run adds the other decode "
+                         "workloads, prefill and the read stream)")
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="llama3_8b",
                     choices=["llama3_8b", "long_context", "shared_prefix", "ragged", "tiny",

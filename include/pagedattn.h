@@ -79,11 +79,25 @@ int pa_version(void);
 
 /*
  * Workspace bytes pa_decode needs for a batch of num_seqs sequences no longer
- * than max_seq_len tokens.  partition_tokens: 0 selects the default (512).
+ * than max_seq_len tokens, whichever decode kernel serves the call (an upper
+ * bound over the kernels).  partition_tokens: 0 selects the default (512).
  * Returns 0 for invalid arguments.
  */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
                                  int max_seq_len, int partition_tokens);
+
+/*
+ * Workspace bytes of the decode kernel that a pa_decode call with these
+ * arguments runs under the current kernel selection (pa_set_decode_path): the
+ * grouped tensor-core kernel needs only its stream-K area (per-CTA partials,
+ * independent of the sequence lengths), the others the [num_seqs, num_q_heads,
+ * partitions] partials.  At most pa_decode_workspace_bytes(...).  Returns 0 for
+ * arguments pa_decode would reject.  Host only; reads no device memory.
+ */
+size_t pa_decode_workspace_bytes_for(int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int max_blocks,
+                                     int num_blocks, int max_seq_len, int dtype,
+                                     int partition_tokens);
 
 /*
  * out[b, hq, :] = sum_t softmax_t(scale * q[b, hq, :] . K[slot_t, hq / G, :])
@@ -108,9 +122,10 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
  *               block_size); 0 = default 512.  Sequences longer than one
  *               partition are processed as independent partitions whose
  *               partial (max, sum, accumulator) are merged by a second pass.
- * workspace     device scratch of at least pa_decode_workspace_bytes(...),
- *               256-byte aligned; contents need not be initialised; it may
- *               not be shared by calls that overlap on the GPU.
+ * workspace     device scratch of at least pa_decode_workspace_bytes_for(...)
+ *               (pa_decode_workspace_bytes(...) always suffices), 256-byte
+ *               aligned; contents need not be initialised; it may not be
+ *               shared by calls that overlap on the GPU.
  * Supported: dtype fp16/bf16, head_dim 64 or 128, block_size 8/16/32/64,
  * num_q_heads a multiple of num_kv_heads.
  */
@@ -127,7 +142,8 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
  * Three decode kernels exist:
  *   grouped tensor-core kernel (tcgen05 + TMA): each CTA reads whole blocks,
  *     all KV heads at once, over an equal share of the batch's tokens;
- *     head_dim 128, num_kv_heads 4 or 8, num_q_heads / num_kv_heads in {1,2,4,8};
+ *     head_dim 128, num_kv_heads in {1,2,4,8,16,32}, num_q_heads / num_kv_heads
+ *     in {1,2,4,8}, num_q_heads <= 64, num_seqs <= 1023;
  *   per-head tensor-core kernel (tcgen05 + TMA): one KV head per work item;
  *     head_dim 128, any grouping;
  *   CUDA-core kernel: every supported shape.
@@ -159,15 +175,19 @@ pa_status pa_set_decode_path(int path);
  * loads the library holds it until the process exits.  It calls no
  * allocating routine.
  *
- *  - Limit: a batch whose pa_decode_workspace_bytes(...) exceeds
+ *  - Limit: a batch whose pa_decode_workspace_bytes_for(...) exceeds
  *    PA_DECODE_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE before
- *    any device work (e.g. 64 sequences x 32 query heads up to 4096 tokens
- *    need about 8.1 MiB; 8 x 64 heads up to 128K tokens need about 65 MiB and
- *    are rejected).  Other errors are those of pa_decode.
+ *    any device work.  The grouped tensor-core kernel (the default where it
+ *    serves the shape) needs at most about 11 MiB whatever the lengths; the
+ *    other kernels need [num_seqs, num_q_heads, partitions] partials, e.g.
+ *    8 sequences x 64 query heads up to 128K tokens about 65 MiB, which is
+ *    rejected.  Other errors are those of pa_decode.
  *  - Set-up: the first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current; this may load the module).
  *    Make that first call before any stream capture.  The current device must
- *    be the device of the buffers and of `stream`.
+ *    be the device of the buffers and of `stream`.  The address is kept per
+ *    device context: after cudaDeviceReset the next call looks it up again
+ *    (so, again, before any capture).
  *  - Sharing: all calls share the one array, which keeps the last call's
  *    contents; nothing in it needs to start at zero.  Calls that overlap on the
  *    GPU (different streams, or different host threads without ordering) race
@@ -220,11 +240,15 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* block_pairs,
  * slot_mapping[b] = slot of token seq_lens[b] - 1 of sequence b (its newest
  * token), block_tables[b][(L-1) / block_size] * block_size + (L-1) % block_size,
  * or -1 when seq_lens[b] == 0 (tutorial §4 PhysicalIndex).  Feeds
- * pa_reshape_and_cache in a decode step.
+ * pa_reshape_and_cache in a decode step.  A negative length, a length past
+ * max_blocks * block_size, or a block id outside [0, num_blocks) also gives -1
+ * and is reported through status_dev (checked mode), so the token is never
+ * written anywhere.  num_blocks * block_size must fit an int32.
  */
 pa_status pa_decode_slots(int32_t* slot_mapping, const int32_t* block_tables,
                           const int32_t* seq_lens, int num_seqs, int max_blocks,
-                          int block_size, cudaStream_t stream);
+                          int block_size, int num_blocks, int32_t* status_dev,
+                          cudaStream_t stream);
 
 /*
  * Decode-step cache write in one launch: pa_decode_slots followed by
@@ -473,6 +497,21 @@ typedef struct {
 pa_status pa_sim_run(const pa_sim_config* cfg, const int32_t* arrival_step,
                      const int32_t* prompt_len, const int32_t* output_len, int num_requests,
                      pa_sim_result* out);
+
+/* ------------------------------------------------------------------------ */
+/* Measurement aid                                                           */
+/* ------------------------------------------------------------------------ */
+/*
+ * A plain read stream over `bytes` bytes of device memory at `src` (16-byte
+ * aligned, bytes a multiple of 16): every byte read once, contiguously, with
+ * no gather and no compute.  Not part of the decode path: timing it in the same
+ * run as pa_decode gives the read bandwidth a kernel reaches on this GPU, next
+ * to which the decode kernels' bandwidth is read.  `sink` (nullable, device) is
+ * incremented only when the XOR of all words read equals 0x9E3779B9, so the
+ * loads cannot be dropped.  Asynchronous on `stream`.
+ */
+pa_status pa_stream_read(const void* src, size_t bytes, unsigned long long* sink,
+                         cudaStream_t stream);
 
 #ifdef __cplusplus
 }

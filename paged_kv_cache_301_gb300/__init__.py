@@ -68,10 +68,37 @@ def pa_decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,
 
 def alloc_workspace(num_seqs, num_q_heads, head_dim, max_seq_len, partition_tokens=0,
                     device="cuda") -> torch.Tensor:
+    """A workspace large enough for any decode kernel (pa_decode_workspace_bytes)."""
     n = pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len, partition_tokens)
     if n == 0:
         raise ValueError("invalid workspace arguments")
     return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def pa_decode_workspace_bytes_for(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                  head_dim: int, block_size: int, max_blocks: int,
+                                  num_blocks: int, max_seq_len: int, dtype: int,
+                                  partition_tokens: int = 0) -> int:
+    """Bytes the decode kernel that serves these arguments needs (0: invalid)."""
+    return int(lib().pa_decode_workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads,
+                                                   head_dim, block_size, max_blocks, num_blocks,
+                                                   max_seq_len, dtype, partition_tokens))
+
+
+def workspace_for(q: torch.Tensor, k_pool: torch.Tensor, block_tables: torch.Tensor,
+                  max_seq_len: int, partition_tokens: int = 0,
+                  strict: bool = True) -> torch.Tensor:
+    """The workspace of exactly the size the decode kernel serving this call
+    needs (pa_decode_workspace_bytes_for, under the current kernel selection).
+    For arguments the library would reject: ValueError, or with strict=False an
+    empty tensor, so that the decode call itself reports the library's status."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_pool.shape
+    n = pa_decode_workspace_bytes_for(B, Hq, Hkv, D, bs, block_tables.shape[1], NB,
+                                      int(max_seq_len), _dtype(q), partition_tokens)
+    if n == 0 and strict:
+        raise ValueError("invalid decode arguments")
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
 
 
 def pa_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
@@ -90,7 +117,8 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor, v_pool: 
     if max_seq_len is None:
         max_seq_len = MB * bs
     if workspace is None:
-        workspace = alloc_workspace(B, Hq, D, max_seq_len, partition_tokens, q.device)
+        workspace = workspace_for(q, k_pool, block_tables, max_seq_len, partition_tokens,
+                                  strict=False)
     st = lib().pa_decode(
         _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens),
         B, Hq, Hkv, D, bs, MB, NB, int(max_seq_len), float(scale), _dtype(q),
@@ -115,7 +143,8 @@ def pa_decode_append(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
     if max_seq_len is None:
         max_seq_len = MB * bs
     if workspace is None:
-        workspace = alloc_workspace(B, Hq, D, max_seq_len, partition_tokens, q.device)
+        workspace = workspace_for(q, k_pool, block_tables, max_seq_len, partition_tokens,
+                                  strict=False)
     st = lib().pa_decode_append(
         _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(key), _ptr(value),
         _ptr(block_tables), _ptr(seq_lens), B, Hq, Hkv, D, bs, MB, NB, int(max_seq_len),
@@ -229,11 +258,13 @@ def pa_swap_blocks(dst_pools: Sequence[torch.Tensor], src_pools: Sequence[torch.
 
 
 def pa_decode_slots(slot_mapping: torch.Tensor, block_tables: torch.Tensor,
-                    seq_lens: torch.Tensor, block_size: int, stream=None) -> torch.Tensor:
-    """slot_mapping[b] = pool slot of token seq_lens[b] - 1 (or -1 for empty)."""
+                    seq_lens: torch.Tensor, block_size: int, num_blocks: int,
+                    status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """slot_mapping[b] = pool slot of token seq_lens[b] - 1 (or -1 for an empty
+    sequence, or, reported through `status`, a bad length or block id)."""
     B, MB = block_tables.shape
     st = lib().pa_decode_slots(_ptr(slot_mapping), _ptr(block_tables), _ptr(seq_lens), B, MB,
-                               block_size, _stream(stream))
+                               block_size, num_blocks, _ptr(status), _stream(stream))
     _check(st, "pa_decode_slots")
     return slot_mapping
 
@@ -278,6 +309,14 @@ def pa_append_tokens(k_pool: torch.Tensor, v_pool: torch.Tensor, key: torch.Tens
         _ptr(slot_mapping), B, 0, Hkv, D, bs, MB, NB, _dtype(k_pool), _ptr(status),
         _stream(stream))
     _check(st, "pa_append_tokens")
+
+
+def pa_stream_read(buf: torch.Tensor, sink: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Read every byte of `buf` once (a plain contiguous read stream, see
+    include/pagedattn.h, pa_stream_read): the read bandwidth measured beside the
+    decode kernels.  sink: optional int64 device tensor of one element."""
+    n = buf.numel() * buf.element_size()
+    _check(lib().pa_stream_read(_ptr(buf), n, _ptr(sink), _stream(stream)), "pa_stream_read")
 
 
 class _SimConfig(ctypes.Structure):
@@ -425,9 +464,9 @@ class BlockManager:
 
 __all__ = [
     "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_append",
-    "pa_decode_workspace_bytes",
+    "pa_decode_workspace_bytes", "pa_decode_workspace_bytes_for", "workspace_for",
     "pa_decode_noalloc", "set_decode_path",
     "alloc_workspace", "pa_reshape_and_cache", "pa_append_tokens", "pa_prefill", "set_prefill_path",
     "pa_copy_blocks_multi", "pa_swap_blocks", "pa_copy_blocks", "pa_decode_slots",
-    "BlockManager", "lib", "simulate_allocator",
+    "BlockManager", "lib", "simulate_allocator", "pa_stream_read",
 ]

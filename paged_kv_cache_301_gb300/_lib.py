@@ -22,6 +22,8 @@ SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [c_int]),
     "pa_version": (c_int, []),
     "pa_decode_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "pa_decode_workspace_bytes_for": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int,
+                                                 c_int, c_int, c_int, c_int]),
     "pa_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                           c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                           c_float, c_int, c_int, c_void_p, c_size_t, c_void_p, c_void_p]),
@@ -49,7 +51,9 @@ SIGNATURES = {
     "pa_append_tokens": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_void_p, c_int, c_int64, c_int, c_int, c_int, c_int, c_int,
                                  c_int, c_void_p, c_void_p]),
-    "pa_decode_slots": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p]),
+    "pa_stream_read": (c_int, [c_void_p, c_size_t, c_void_p, c_void_p]),
+    "pa_decode_slots": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                c_void_p, c_void_p]),
     "pa_bm_create": (c_int, [c_int, c_int, c_void_p, ctypes.POINTER(c_void_p)]),
     "pa_bm_destroy": (None, [c_void_p]),
     "pa_sim_run": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p]),

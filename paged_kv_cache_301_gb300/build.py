@@ -29,6 +29,7 @@ SOURCES = [
     "pa_decode_noalloc.cu",
     "pa_decode_tc.cu",
     "pa_decode_tcg.cu", "pa_blocks.cu", "pa_prefill_tc.cu", "pa_prefill_simt.cu",
+    "pa_stream.cu",
 ]
 HEADERS = [
     os.path.join(ROOT, "include", "pagedattn.h"),

@@ -8,22 +8,48 @@ namespace pa {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-WorkspaceLayout workspace_layout(int B, int Hq, int D, int P) {
+// Each kernel lays out only what it uses, from offset 0: the grouped kernel its
+// stream-K area; the per-head kernel the work queue, the (sequence, partition)
+// items and the [B, Hq, P] partials; the CUDA-core kernel the partials.
+WorkspaceLayout workspace_layout(DecodeKernel k, int B, int Hq, int D, int P) {
   const size_t rows = (size_t)B * Hq * P;
-  WorkspaceLayout w;
-  w.queue_off = 0;                                   // work-queue counters
-  w.items_off = 256;                                 // (sequence, partition) pairs
-  w.m_off = w.items_off + align256((size_t)B * P * 2 * sizeof(int));
+  WorkspaceLayout w = {};
+  if (k == DecodeKernel::kGrouped) {
+    w.sk_off = 0;
+    w.total = sk_layout(B, Hq).total;
+    return w;
+  }
+  size_t off = 0;
+  if (k == DecodeKernel::kPerHead) {
+    w.queue_off = 0;                                 // work-queue counters
+    w.items_off = 256;                               // (sequence, partition) pairs
+    off = w.items_off + align256((size_t)B * P * 2 * sizeof(int));
+  }
+  w.m_off = off;
   w.l_off = w.m_off + align256(rows * sizeof(float));
   w.acc_off = w.l_off + align256(rows * sizeof(float));
-  w.sk_off = w.acc_off + align256(rows * D * sizeof(float));
-  w.total = w.sk_off + sk_layout(B, Hq).total;
+  w.total = w.acc_off + align256(rows * D * sizeof(float));
   return w;
 }
 
+// Process-wide kernel choice: a switch for tests and measurements (see
+// pa_set_decode_path), read once per call.
 static int g_decode_path = PA_DECODE_AUTO;
 
 static bool valid_partition(int pt) { return pt >= 128 && pt <= 1024 && pt % 128 == 0; }
+
+// The kernel a call runs: the grouped tensor-core kernel where it serves the
+// shape, else the per-head tensor-core kernel (head_dim 128), else the CUDA-core
+// kernel; kNone when the path setting asks for a tensor-core kernel that does
+// not serve the call.
+DecodeKernel choose_decode_kernel(const DecodeParams& p, int path) {
+  if (path != PA_DECODE_SIMT && path != PA_DECODE_TC_HEAD && tcg_supported(p))
+    return DecodeKernel::kGrouped;
+  const bool per_head = path != PA_DECODE_SIMT && tc_supported(p);
+  if ((path == PA_DECODE_TC || path == PA_DECODE_TC_HEAD) && !per_head)
+    return DecodeKernel::kNone;
+  return per_head ? DecodeKernel::kPerHead : DecodeKernel::kSimt;
+}
 
 }  // namespace pa
 
@@ -53,7 +79,54 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int h
       !valid_partition(pt))
     return 0;
   const int P = max(1, num_partitions(max_seq_len, pt));
-  return workspace_layout(num_seqs, num_q_heads, head_dim, P).total;
+  // enough for whichever kernel runs
+  const size_t a = workspace_layout(DecodeKernel::kGrouped, num_seqs, num_q_heads, head_dim, P).total;
+  const size_t b = workspace_layout(DecodeKernel::kPerHead, num_seqs, num_q_heads, head_dim, P).total;
+  return a > b ? a : b;
+}
+
+// Host-side checks shared by pa_decode and the workspace query: fills the
+// shape fields of p; returns PA_OK or the status pa_decode would return.
+static pa_status check_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_blocks, int num_blocks, int max_seq_len,
+                             int dtype, int partition_tokens, DecodeParams* p) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks <= 0 ||
+      num_blocks <= 0 || max_seq_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+  if (!(head_dim == 64 || head_dim == 128)) return PA_ERR_UNSUPPORTED;
+  if (!(block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64))
+    return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_FLOAT16 && dtype != PA_BFLOAT16) return PA_ERR_UNSUPPORTED;
+  const int pt = partition_tokens == 0 ? kDefaultPartitionTokens : partition_tokens;
+  if (!valid_partition(pt) || pt % block_size) return PA_ERR_INVALID_ARG;
+  if ((long long)max_seq_len > (long long)max_blocks * block_size) return PA_ERR_INVALID_ARG;
+  *p = DecodeParams{};
+  p->B = num_seqs;
+  p->Hq = num_q_heads;
+  p->Hkv = num_kv_heads;
+  p->D = head_dim;
+  p->bs = block_size;
+  p->max_blocks = max_blocks;
+  p->num_blocks = num_blocks;
+  p->max_seq_len = max_seq_len;
+  p->dtype = dtype;
+  p->PT = pt;
+  p->P = max(1, num_partitions(max_seq_len, pt));
+  return PA_OK;
+}
+
+extern "C" size_t pa_decode_workspace_bytes_for(int num_seqs, int num_q_heads, int num_kv_heads,
+                                                int head_dim, int block_size, int max_blocks,
+                                                int num_blocks, int max_seq_len, int dtype,
+                                                int partition_tokens) {
+  DecodeParams p;
+  if (check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks,
+                  num_blocks, max_seq_len, dtype, partition_tokens, &p) != PA_OK)
+    return 0;
+  const DecodeKernel k = choose_decode_kernel(p, g_decode_path);
+  if (k == DecodeKernel::kNone) return 0;
+  return workspace_layout(k, p.B, p.Hq, p.D, p.P).total;
 }
 
 // pa_decode, optionally preceded by the decode-step cache write of
@@ -67,17 +140,10 @@ static pa_status decode_impl(void* out, const void* q, const void* k_pool, const
                              int block_size, int max_blocks, int num_blocks, int max_seq_len,
                              float scale, int dtype, int partition_tokens, void* workspace,
                              size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream) {
-  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks <= 0 ||
-      num_blocks <= 0 || max_seq_len < 0)
-    return PA_ERR_INVALID_ARG;
-  if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
-  if (!(head_dim == 64 || head_dim == 128)) return PA_ERR_UNSUPPORTED;
-  if (!(block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64))
-    return PA_ERR_UNSUPPORTED;
-  if (dtype != PA_FLOAT16 && dtype != PA_BFLOAT16) return PA_ERR_UNSUPPORTED;
-  const int pt = partition_tokens == 0 ? kDefaultPartitionTokens : partition_tokens;
-  if (!valid_partition(pt) || pt % block_size) return PA_ERR_INVALID_ARG;
-  if ((long long)max_seq_len > (long long)max_blocks * block_size) return PA_ERR_INVALID_ARG;
+  DecodeParams p;
+  pa_status st = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             max_blocks, num_blocks, max_seq_len, dtype, partition_tokens, &p);
+  if (st != PA_OK) return st;
   if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
@@ -86,30 +152,19 @@ static pa_status decode_impl(void* out, const void* q, const void* k_pool, const
   const bool append = new_k != nullptr || new_v != nullptr;
   if (append && (!new_k || !new_v || (((uintptr_t)new_k | (uintptr_t)new_v) & 15u) != 0))
     return PA_ERR_INVALID_ARG;
-  const int P = max(1, num_partitions(max_seq_len, pt));
-  const WorkspaceLayout wl = workspace_layout(num_seqs, num_q_heads, head_dim, P);
+  const DecodeKernel kernel = choose_decode_kernel(p, g_decode_path);
+  if (kernel == DecodeKernel::kNone) return PA_ERR_UNSUPPORTED;
+  const WorkspaceLayout wl = workspace_layout(kernel, num_seqs, num_q_heads, head_dim, p.P);
   if (!workspace || workspace_bytes < wl.total || ((uintptr_t)workspace & 255u) != 0)
     return PA_ERR_WORKSPACE;
 
-  DecodeParams p;
   p.out = out;
   p.q = q;
   p.k_pool = k_pool;
   p.v_pool = v_pool;
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
-  p.B = num_seqs;
-  p.Hq = num_q_heads;
-  p.Hkv = num_kv_heads;
-  p.D = head_dim;
-  p.bs = block_size;
-  p.max_blocks = max_blocks;
-  p.num_blocks = num_blocks;
-  p.max_seq_len = max_seq_len;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  p.dtype = dtype;
-  p.PT = pt;
-  p.P = P;
   char* ws = static_cast<char*>(workspace);
   p.ws_m = reinterpret_cast<float*>(ws + wl.m_off);
   p.ws_l = reinterpret_cast<float*>(ws + wl.l_off);
@@ -118,16 +173,13 @@ static pa_status decode_impl(void* out, const void* q, const void* k_pool, const
   p.new_k = nullptr;
   p.new_v = nullptr;
 
-  const int path = g_decode_path;
-  const bool grouped = path != PA_DECODE_SIMT && path != PA_DECODE_TC_HEAD && tcg_supported(p);
-  if (grouped) {
+  if (kernel == DecodeKernel::kGrouped) {
     p.new_k = new_k;
     p.new_v = new_v;
     return launch_decode_tcg(p, ws + wl.sk_off, stream);
   }
-  const bool per_head = path != PA_DECODE_SIMT && tc_supported(p);
-  if ((path == PA_DECODE_TC || path == PA_DECODE_TC_HEAD) && !per_head) return PA_ERR_UNSUPPORTED;
-  pa_status st;
+  const bool per_head = kernel == DecodeKernel::kPerHead;
+  const int P = p.P;
   if (append) {
     st = pa_append_tokens(const_cast<void*>(k_pool), const_cast<void*>(v_pool), new_k, new_v,
                           block_tables, seq_lens, nullptr, num_seqs, 0, num_kv_heads, head_dim,

@@ -64,21 +64,32 @@ copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
   for (; v < block_vecs; v += 256) to[v] = from[v];
 }
 
+// Slot of each sequence's newest token, or -1.  A length past the table or a
+// block id outside [0, num_blocks) gives -1 and is reported (checked mode), as
+// in append_tokens_kernel, so that a bad table entry never turns into a slot
+// that a later cache write would silently treat as padding or write through.
 __global__ void decode_slots_kernel(int32_t* __restrict__ slot_mapping,
                                     const int32_t* __restrict__ block_tables,
                                     const int32_t* __restrict__ seq_lens, int num_seqs,
-                                    int max_blocks, int block_size) {
+                                    int max_blocks, int block_size, int num_blocks,
+                                    int32_t* status_dev) {
   allow_next_grid();
   wait_prior_grid();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= num_seqs) return;
   const int len = seq_lens[b];
   if (len <= 0 || len > max_blocks * block_size) {
+    if (len != 0) report(status_dev, PA_ERR_BAD_BLOCK_ID);
     slot_mapping[b] = -1;
     return;
   }
   const int pos = len - 1;
   const int32_t blk = block_tables[(int64_t)b * max_blocks + pos / block_size];
+  if (blk < 0 || blk >= num_blocks) {
+    report(status_dev, PA_ERR_BAD_BLOCK_ID);
+    slot_mapping[b] = -1;
+    return;
+  }
   slot_mapping[b] = blk * block_size + pos % block_size;
 }
 
@@ -177,13 +188,17 @@ extern "C" pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* b
 
 extern "C" pa_status pa_decode_slots(int32_t* slot_mapping, const int32_t* block_tables,
                                      const int32_t* seq_lens, int num_seqs, int max_blocks,
-                                     int block_size, cudaStream_t stream) {
-  if (num_seqs < 0 || max_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
+                                     int block_size, int num_blocks, int32_t* status_dev,
+                                     cudaStream_t stream) {
+  if (num_seqs < 0 || max_blocks <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  // every slot of the pool is an int32
+  if ((long long)num_blocks * block_size > 0x7FFFFFFFll) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   if (!slot_mapping || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
   if (launch_pdl(decode_slots_kernel, dim3((unsigned)((num_seqs + 127) / 128)), 128, 0, stream,
-                 slot_mapping, block_tables, seq_lens, num_seqs, max_blocks,
-                 block_size) != cudaSuccess)
+                 slot_mapping, block_tables, seq_lens, num_seqs, max_blocks, block_size,
+                 num_blocks, status_dev) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }

@@ -32,11 +32,16 @@ struct DecodeParams {
   const void* new_v;
 };
 
-// Workspace carve-up; identical for every decode kernel.
+// The decode kernels; which one serves a call depends on its shape and on the
+// process-wide path setting (pa_set_decode_path).
+enum class DecodeKernel { kGrouped, kPerHead, kSimt, kNone };
+DecodeKernel choose_decode_kernel(const DecodeParams& p, int path);
+
+// Workspace carve-up of one kernel (offsets of the parts it uses; total bytes).
 struct WorkspaceLayout {
   size_t queue_off, items_off, m_off, l_off, acc_off, sk_off, total;
 };
-WorkspaceLayout workspace_layout(int B, int Hq, int D, int P);
+WorkspaceLayout workspace_layout(DecodeKernel k, int B, int Hq, int D, int P);
 
 pa_status launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 pa_status launch_combine(const DecodeParams& p, cudaStream_t stream);

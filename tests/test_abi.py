@@ -112,7 +112,8 @@ def test_workspace_size(lib):
     per_head = 256 + a(64 * P * 8) + 2 * a(rows * 4) + a(rows * 128 * 4)
     parts = 160 * 2 * 32
     grouped = a(65 * 4) + 2 * a(parts * 4) + a(parts * 128 * 4)
-    assert n == per_head + grouped
+    # enough for whichever kernel runs (each lays out its own parts from 0)
+    assert n == max(per_head, grouped)
     assert lib.pa_decode_workspace_bytes(64, 32, 128, 4096, 100) == 0
     assert lib.pa_decode_workspace_bytes(-1, 32, 128, 4096, 0) == 0
 
@@ -128,5 +129,35 @@ def test_cache_argument_checks(lib):
     assert g(16, 16, 16, 0, 8, 128, 16, 8, 1, None, None) == 0
     assert g(16, 16, None, 2, 8, 128, 16, 8, 1, None, None) == 1
     s = lib.pa_decode_slots
-    assert s(16, 16, 16, 0, 4, 16, None) == 0
-    assert s(None, 16, 16, 3, 4, 16, None) == 1
+    assert s(16, 16, 16, 0, 4, 16, 8, None, None) == 0
+    assert s(None, 16, 16, 3, 4, 16, 8, None, None) == 1
+    assert s(16, 16, 16, 3, 4, 16, 0, None, None) == 1            # no pool
+    assert s(16, 16, 16, 3, 4, 64, 1 << 26, None, None) == 1      # slots overflow int32
+
+
+def _align(x):
+    return (x + 255) // 256 * 256
+
+
+def test_workspace_size_of_the_cuda_core_kernel(lib):
+    """pa_decode_workspace_bytes_for sizes the kernel that runs: with the CUDA-core
+    kernel selected, [B, Hq, P] maxima and sums plus [B, Hq, P, D] accumulators
+    (P = 512-token partitions of the longest sequence); never above the
+    kernel-independent bound; 0 for arguments pa_decode would reject."""
+    assert lib.pa_set_decode_path(1) == 0
+    try:
+        f = lib.pa_decode_workspace_bytes_for
+        for B, Hq, Hkv, D, bs, mx in ((64, 32, 8, 128, 16, 4096), (8, 64, 8, 128, 32, 131072),
+                                      (3, 4, 4, 64, 8, 1)):
+            P = -(-mx // 512)
+            rows = B * Hq * P
+            want = 2 * _align(4 * rows) + _align(4 * rows * D)
+            got = f(B, Hq, Hkv, D, bs, -(-mx // bs), 1000, mx, 1, 0)
+            assert got == want
+            assert got <= lib.pa_decode_workspace_bytes(B, Hq, D, mx, 0)
+        assert f(4, 6, 4, 128, 16, 8, 100, 128, 1, 0) == 0           # Hq % Hkv
+        assert f(4, 8, 4, 96, 16, 8, 100, 128, 1, 0) == 0            # head_dim
+        assert f(4, 8, 4, 128, 16, 8, 100, 129, 1, 0) == 0           # longer than the table
+        assert f(4, 8, 4, 128, 16, 8, 100, 128, 1, 100) == 0         # partition size
+    finally:
+        lib.pa_set_decode_path(0)

@@ -27,6 +27,10 @@ def test_reference_arm_line():
     assert BASE_KEYS <= set(d)
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 3
     assert d["config"]["workload"] == "llama3_8b" and d["value"] > 0
+    # the same workload description as the native arm's line
+    assert {"num_seqs", "seq_lens", "total_tokens", "num_blocks", "kv_bytes_per_step"} <= \
+        set(d["config"])
+    assert d["config"]["num_seqs"] == 64 and d["config"]["total_tokens"] == 149573
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
 
@@ -38,8 +42,19 @@ def test_native_arm_line():
     assert d["n_gpus"] == 1 and d["steps"] == 20 and d["warmup"] == 5
     assert d["scaling"] == "weak" and d["higher_is_better"] is True and d["dtype"] == "bf16"
     assert d["config"]["workload"] == "llama3_8b" and d["value"] > 0
-    # the step is one pa_decode_append call: main + combine on the grouped kernel
-    assert d["gpu_launches"] == 2 * 20
+    # the step is one pa_decode_append call: main + combine on the grouped kernel;
+    # the value is the median over the repeats of the 20-step block
+    assert d["gpu_launches_per_step"] == 2 and d["repeats"] >= 25
+    assert d["gpu_launches"] == 2 * 20 * d["repeats"]
+    # every other decode workload, prefill and the read stream in the same line
+    assert {"long_context", "shared_prefix", "ragged", "prefill"} <= set(d["workloads"])
+    for name in ("long_context", "shared_prefix", "ragged"):
+        x = d["workloads"][name]
+        assert x["config"]["workload"] == name and x["value"] > 0 and x["tokens_per_s"] > 0
+        assert x["roofline"]["bound"] == "hbm" and 0 < x["roofline"]["frac"] < 1.5
+    assert d["workloads"]["prefill"]["roofline"]["bound"] == "tensor"
+    assert d["stream_read"]["gbs"] > 0
+    assert d["l2_flushed"]["avg_launch_ms"] > 0
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0 < r["frac"] < 1.5
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3

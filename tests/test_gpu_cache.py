@@ -99,15 +99,47 @@ def test_copy_blocks_bit_exact(pa, bs):
 
 def test_decode_slots_match_block_manager(pa):
     initial, steps, final = scenarios.ragged_steps(syn.RAGGED, 16, 3, num_seqs=64)
+    nb = initial.num_blocks
     for st in steps:
         out = torch.empty(len(st.seq_lens), dtype=torch.int32, device="cuda")
-        pa.pa_decode_slots(out, i32(st.block_tables), i32(st.seq_lens), 16)
+        pa.pa_decode_slots(out, i32(st.block_tables), i32(st.seq_lens), 16, nb)
         assert np.array_equal(out.cpu().numpy(), st.slot_mapping)
     lens = steps[0].seq_lens.copy()
     lens[:5] = 0
     out = torch.empty(len(lens), dtype=torch.int32, device="cuda")
-    pa.pa_decode_slots(out, i32(steps[0].block_tables), i32(lens), 16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_decode_slots(out, i32(steps[0].block_tables), i32(lens), 16, nb, status=status)
     assert (out.cpu().numpy()[:5] == -1).all()
+    assert int(status.item()) == 0              # empty sequences are not errors
+
+
+def test_decode_slots_checked_mode_poisoned_table(pa):
+    """A table entry outside the pool (negative, or num_blocks and beyond) where a
+    newest token lands gives slot -1 and PA_ERR_BAD_BLOCK_ID; other slots are
+    still those of the block manager."""
+    initial, steps, final = scenarios.ragged_steps(syn.RAGGED, 16, 1, num_seqs=64)
+    st = steps[0]
+    nb = initial.num_blocks
+    tables = st.block_tables.copy()
+    last = (st.seq_lens.astype(np.int64) - 1) // 16
+    bad = {3: -7, 10: nb, 20: nb + 1000}
+    for b, v in bad.items():
+        tables[b, last[b]] = v
+    out = torch.empty(len(st.seq_lens), dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_decode_slots(out, i32(tables), i32(st.seq_lens), 16, nb, status=status)
+    got = out.cpu().numpy()
+    want = st.slot_mapping.copy()
+    for b in bad:
+        want[b] = -1
+    assert np.array_equal(got, want)
+    assert int(status.item()) == 5
+    # a length past the table is reported the same way
+    lens = st.seq_lens.copy()
+    lens[7] = tables.shape[1] * 16 + 1
+    status.zero_()
+    pa.pa_decode_slots(out, i32(st.block_tables), i32(lens), 16, nb, status=status)
+    assert int(out[7].item()) == -1 and int(status.item()) == 5
 
 
 @pytest.mark.parametrize("bs", [8, 16, 64])
@@ -166,7 +198,7 @@ def test_ragged_continuous_batching_steps(pa, bs):
     for i, st in enumerate(steps):
         tables, lens = i32(st.block_tables), i32(st.seq_lens)
         slots = torch.empty(B, dtype=torch.int32, device="cuda")
-        pa.pa_decode_slots(slots, tables, lens, bs)
+        pa.pa_decode_slots(slots, tables, lens, bs, initial.num_blocks)
         pa.pa_reshape_and_cache(dev.k_pool, dev.v_pool, to_dev(st.key, dt), to_dev(st.value, dt),
                                 slots)
         out = dev.decode(pa, tables=tables, lens=lens, max_seq_len=int(st.seq_lens.max()))

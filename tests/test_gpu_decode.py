@@ -295,3 +295,33 @@ def test_more_kv_heads_per_block_ragged(pa, hq, hkv, bs):
     batch = scenarios.fixed_batch(w)
     got = widen(DeviceBatch(batch).decode(pa))
     assert_close(got, scenarios.decode_f64(batch), f"Hq={hq} Hkv={hkv} bs={bs}")
+
+
+def test_workspace_of_exactly_the_grouped_kernels_size(pa):
+    """The grouped kernel's workspace is its stream-K area only (tile prefix,
+    per-CTA (max, sum) and accumulators of up to 160 CTAs x 2 segments), whatever
+    the lengths: pa_decode runs with exactly that many bytes and refuses one
+    fewer; the result matches the oracle."""
+    if pa.decode_path != "tc":
+        pytest.skip("the grouped kernel's layout")
+    w = syn.LLAMA3_8B.__class__(**{**syn.LLAMA3_8B.__dict__, "num_seqs": 12, "hi": 1500,
+                                   "seed": 77})
+    batch = scenarios.fixed_batch(w)
+    dev = DeviceBatch(batch)
+    B, Hq, D = dev.q.shape
+    max_len = int(batch.seq_lens.max())
+    n = pa.pa_decode_workspace_bytes_for(B, Hq, w.num_kv_heads, D, w.block_size,
+                                         dev.tables.shape[1], batch.num_blocks, max_len, 1)
+    parts = 160 * 2 * Hq
+    assert n == (-(-4 * (B + 1) // 256) * 256) + 2 * (-(-4 * parts // 256) * 256) + \
+        (-(-4 * parts * D // 256) * 256)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dev.q)
+    pa.pa_decode(out, dev.q, dev.k_pool, dev.v_pool, dev.tables, dev.lens, batch.scale,
+                 max_seq_len=max_len, workspace=ws)
+    torch.cuda.synchronize()
+    assert_close(widen(out), scenarios.decode_f64(batch), "exact grouped workspace")
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.pa_decode(out, dev.q, dev.k_pool, dev.v_pool, dev.tables, dev.lens, batch.scale,
+                     max_seq_len=max_len, workspace=ws[:n - 256])
+    assert e.value.status == 3
