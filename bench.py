@@ -212,17 +212,6 @@ def recorded_traffic(workload_name: str, kernel: str):
     return None
 
 
-def decode_kernel_for(w, kernel: str) -> str:
-    """Which decode kernel runs (mirrors the library's selection)."""
-    grouped = (w.head_dim == 128 and w.num_kv_heads in (1, 2, 4, 8, 16, 32)
-               and w.group in (1, 2, 4, 8) and w.num_q_heads <= 64 and w.num_seqs <= 1023)
-    if kernel in ("auto", "tc"):
-        if grouped:
-            return "tcg"
-        return "tc_head" if w.head_dim == 128 else "simt"
-    return kernel
-
-
 class NativeStep:
     """Device state of one replica: pool, tables, inputs; run() = one step."""
 
@@ -283,7 +272,9 @@ class NativeStep:
         pa.set_decode_path(kernel)
         self.ws = pa.workspace_for(q, self.k_pool, tables, self.max_seq_len, partition_tokens)
         P = -(-self.max_seq_len // (partition_tokens or 512))
-        self.kernel = decode_kernel_for(w, kernel)
+        # the kernel the library runs for this call (its own selection)
+        self.kernel = {"grouped": "tcg", "per_head": "tc_head", "simt": "simt"}[
+            pa.decode_kernel_for(q, self.k_pool, tables, self.max_seq_len, partition_tokens)]
         # append_tokens, then decode: main + combine (grouped), plan + main
         # (+ combine) (per-head), main (+ combine) (CUDA cores).  The fused step
         # (pa_decode_append) writes the new tokens inside the grouped main kernel.

@@ -143,7 +143,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
  *   grouped tensor-core kernel (tcgen05 + TMA): each CTA reads whole blocks,
  *     all KV heads at once, over an equal share of the batch's tokens;
  *     head_dim 128, num_kv_heads in {1,2,4,8,16,32}, num_q_heads / num_kv_heads
- *     in {1,2,4,8}, num_q_heads <= 64, num_seqs <= 1023;
+ *     in {1,2,4,8}, num_q_heads <= 64, num_seqs <= 16384;
  *   per-head tensor-core kernel (tcgen05 + TMA): one KV head per work item;
  *     head_dim 128, any grouping;
  *   CUDA-core kernel: every supported shape.
@@ -159,6 +159,19 @@ typedef enum pa_decode_path {
   PA_DECODE_AUTO = 0, PA_DECODE_SIMT = 1, PA_DECODE_TC = 2, PA_DECODE_TC_HEAD = 3
 } pa_decode_path;
 pa_status pa_set_decode_path(int path);
+
+/*
+ * Which decode kernel a pa_decode call with these arguments runs under the
+ * current selection: PA_KERNEL_GROUPED, PA_KERNEL_PER_HEAD or PA_KERNEL_SIMT;
+ * -1 for arguments pa_decode rejects (or a tensor-core selection that no
+ * tensor-core kernel serves).  Host only; reads no device memory.
+ */
+typedef enum pa_decode_kernel {
+  PA_KERNEL_GROUPED = 0, PA_KERNEL_PER_HEAD = 1, PA_KERNEL_SIMT = 2
+} pa_decode_kernel;
+int pa_decode_kernel_for(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int max_blocks, int num_blocks, int max_seq_len,
+                         int dtype, int partition_tokens);
 
 /*
  * pa_decode for callers that cannot allocate device memory.  The pages have no

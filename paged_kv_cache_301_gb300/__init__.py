@@ -177,6 +177,18 @@ def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
 
 
 DECODE_PATHS = {"auto": 0, "simt": 1, "tc": 2, "tc_head": 3}
+DECODE_KERNELS = {0: "grouped", 1: "per_head", 2: "simt"}
+
+
+def decode_kernel_for(q: torch.Tensor, k_pool: torch.Tensor, block_tables: torch.Tensor,
+                      max_seq_len: int, partition_tokens: int = 0) -> Optional[str]:
+    """Name of the decode kernel ("grouped", "per_head", "simt") that pa_decode
+    runs for these arguments under the current selection; None if rejected."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_pool.shape
+    k = lib().pa_decode_kernel_for(B, Hq, Hkv, D, bs, block_tables.shape[1], NB,
+                                   int(max_seq_len), _dtype(q), partition_tokens)
+    return DECODE_KERNELS.get(k)
 
 
 def set_decode_path(name: str) -> None:
@@ -465,7 +477,7 @@ class BlockManager:
 __all__ = [
     "FLOAT16", "BFLOAT16", "PagedAttnError", "pa_decode", "pa_decode_append",
     "pa_decode_workspace_bytes", "pa_decode_workspace_bytes_for", "workspace_for",
-    "pa_decode_noalloc", "set_decode_path",
+    "pa_decode_noalloc", "set_decode_path", "decode_kernel_for",
     "alloc_workspace", "pa_reshape_and_cache", "pa_append_tokens", "pa_prefill", "set_prefill_path",
     "pa_copy_blocks_multi", "pa_swap_blocks", "pa_copy_blocks", "pa_decode_slots",
     "BlockManager", "lib", "simulate_allocator", "pa_stream_read",

@@ -40,6 +40,8 @@ SIGNATURES = {
     "pa_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_void_p, c_void_p]),
     "pa_set_decode_path": (c_int, [c_int]),
+    "pa_decode_kernel_for": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                     c_int, c_int]),
     "pa_set_prefill_path": (c_int, [c_int]),
     "pa_prefill": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                            c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,

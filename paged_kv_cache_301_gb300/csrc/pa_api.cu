@@ -129,6 +129,21 @@ extern "C" size_t pa_decode_workspace_bytes_for(int num_seqs, int num_q_heads, i
   return workspace_layout(k, p.B, p.Hq, p.D, p.P).total;
 }
 
+extern "C" int pa_decode_kernel_for(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int max_blocks, int num_blocks,
+                                    int max_seq_len, int dtype, int partition_tokens) {
+  DecodeParams p;
+  if (check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks,
+                  num_blocks, max_seq_len, dtype, partition_tokens, &p) != PA_OK)
+    return -1;
+  switch (choose_decode_kernel(p, g_decode_path)) {
+    case DecodeKernel::kGrouped: return PA_KERNEL_GROUPED;
+    case DecodeKernel::kPerHead: return PA_KERNEL_PER_HEAD;
+    case DecodeKernel::kSimt: return PA_KERNEL_SIMT;
+    default: return -1;
+  }
+}
+
 // pa_decode, optionally preceded by the decode-step cache write of
 // pa_append_tokens (new_k / new_v non-null): fused into the grouped tensor-core
 // kernel where that kernel runs, two launches otherwise.  Every argument is

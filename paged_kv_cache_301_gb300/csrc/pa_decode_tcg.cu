@@ -18,11 +18,16 @@
 // P' is stored as two storage-type terms (hi + lo, ~16 significant bits).
 //
 // Work split (stream-K): the batch is a sequence of token tiles, each sequence
-// padded to whole tiles; CTA c of the persistent grid takes the tiles
-// [c*T/grid, (c+1)*T/grid).  A sequence that lies inside one CTA's range is
-// written directly; a sequence cut by range boundaries leaves one partial
-// (max, sum, accumulator) per CTA, merged by the combine kernel.  Every CTA gets
-// the same number of tiles to within one, whatever the length mix.
+// padded to whole tiles.  A sequence weighs kStartWeight + its tiles (starting
+// a sequence costs a CTA about one tile's time: its epilogue and the next
+// sequence's first copies), and CTA c of the persistent grid takes the tiles
+// whose weighted positions fall in [c*W/grid, (c+1)*W/grid), W the batch's
+// total weight.  A sequence that lies inside one CTA's range is written
+// directly; a sequence cut by range boundaries leaves one partial (max, sum,
+// accumulator) per CTA, merged by the combine kernel.  Every CTA gets the same
+// weight to within one, whatever the length mix.  Each CTA keeps in shared
+// memory only the window of sequences its range meets, so the batch size is
+// not bounded by shared memory.
 //
 // Roles (192 threads, one CTA per SM): warp 0 issues TMA, warp 1 issues MMA,
 // warps 2-5 run the softmax and the epilogue (and, in pa_decode_append, the
@@ -50,32 +55,10 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 232448 - 1024;   // per-block limit minus alignment slack
-constexpr int kMaxSeqs = 1023;                 // batch size served (tile prefix in smem)
-constexpr int kTailReserve = 10 * 1024;
+constexpr int kStartWeight = 1;              // a sequence start weighs one tile in the split
+constexpr int kWin = 1024;                   // sequences of one CTA's range (shared memory)
+constexpr int kMaxSeqs = 16384;              // batch size served: B / grid + 2 <= kWin
 
-template <int H, int G>
-struct Geo {
-  static constexpr int Hq = H * G;
-  static constexpr int N = (Hq + 15) / 16 * 16;
-  static constexpr int TT = kRows / H;                   // tokens per tile
-  static constexpr int kQBytes = N * 256;
-  // For N = 64, Q and P' are single-buffered and the room goes to a fifth ring
-  // stage (measured on GB300: long-context decode 90% -> 95% of the HBM peak).
-  // For N = 32 the same trade (six stages) measured slower (82% -> 79.5%): the
-  // softmax then waits for the previous P'.V before writing P'.
-  static constexpr int kQBufs = N >= 64 ? 1 : 2;
-  static constexpr int kPBufs = N >= 64 ? 1 : 2;
-  static constexpr int kPHalf = N * 256;
-  static constexpr int kPBytes = 2 * kPHalf;
-  // as many 32 KB ring stages as the shared memory left over allows
-  static constexpr int kFree = kSmemBudget - kTailReserve - kQBufs * kQBytes - kPBufs * kPBytes;
-  static constexpr int kStages = kFree / kStage > kMaxStages ? kMaxStages : kFree / kStage;
-  static constexpr uint32_t kTmemCols = 4 * N < 64 ? 64 : 4 * N;
-  static constexpr int kRingOff = 0;
-  static constexpr int kQOff = kStages * kStage;
-  static constexpr int kPOff = kQOff + kQBufs * kQBytes;
-  static constexpr int kTailOff = kPOff + kPBufs * kPBytes;
-};
 
 struct SegInfo {
   int b, L, j0, j1;       // sequence, its length, tile range [j0, j1) within it
@@ -101,10 +84,42 @@ struct Tail {
   float alpha[2][N];
   alignas(16) float lred[4][N];
   float m_fin[N];
-  int prefix[kMaxSeqs + 1];   // tiles before sequence b; prefix[B] = all tiles
-  int scan[4];
+  // The CTA's window: the non-empty sequences whose tiles meet its range, in
+  // batch order.  Entry k is sequence win_b[k], whose tiles are the batch tiles
+  // [win_tp[k], win_tp[k+1]).
+  int win_b[kWin];
+  int win_tp[kWin + 1];
+  int nwin;
+  int cut[2];                 // the CTA's tile range [cut[0], cut[1])
+  int win_n[2];               // non-empty sequences before the window's first / after its last
+  int scan[2][4];
   uint32_t tmem_base;
   int abort_flag;
+};
+
+template <int H, int G>
+struct Geo {
+  static constexpr int Hq = H * G;
+  static constexpr int N = (Hq + 15) / 16 * 16;
+  static constexpr int TT = kRows / H;                   // tokens per tile
+  static constexpr int kQBytes = N * 256;
+  // For N = 64, Q and P' are single-buffered and the room goes to a fifth ring
+  // stage (measured on GB300: long-context decode 90% -> 95% of the HBM peak).
+  // For N = 32 the same trade (six stages) measured slower (82% -> 79.5%): the
+  // softmax then waits for the previous P'.V before writing P'.
+  static constexpr int kQBufs = N >= 64 ? 1 : 2;
+  static constexpr int kPBufs = N >= 64 ? 1 : 2;
+  static constexpr int kPHalf = N * 256;
+  static constexpr int kPBytes = 2 * kPHalf;
+  // as many 32 KB ring stages as the shared memory left over allows
+  static constexpr int kFree =
+      kSmemBudget - (int)sizeof(Tail<N>) - kQBufs * kQBytes - kPBufs * kPBytes;
+  static constexpr int kStages = kFree / kStage > kMaxStages ? kMaxStages : kFree / kStage;
+  static constexpr uint32_t kTmemCols = 4 * N < 64 ? 64 : 4 * N;
+  static constexpr int kRingOff = 0;
+  static constexpr int kQOff = kStages * kStage;
+  static constexpr int kPOff = kQOff + kQBufs * kQBytes;
+  static constexpr int kTailOff = kPOff + kPBufs * kPBytes;
 };
 
 template <int DT, int H, int G>
@@ -115,6 +130,7 @@ constexpr int smem_bytes() {
 struct SkParams {
   DecodeParams p;
   int* tile_prefix;         // [B + 1] tiles before sequence b (written by CTA 0 for the combine)
+  int* weight_prefix;       // [B + 1] weight before sequence b (written by CTA 0 for the combine)
   float* part_m;            // [grid * 2 * Hq]
   float* part_l;
   float* part_acc;          // [grid * 2 * Hq * D]
@@ -125,9 +141,14 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
   return L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
 }
 
-// First tile of CTA c's range (T tiles over `grid` CTAs; c * T < 2^31 here).
-__device__ __forceinline__ int range_start(int c, int T, int grid) {
-  return (int)((unsigned)c * (unsigned)T / (unsigned)grid);
+// Start of CTA c's share of W units over `grid` CTAs.
+__device__ __forceinline__ int range_start(int c, int W, int grid) {
+  return (int)((unsigned long long)c * (unsigned)W / (unsigned)grid);
+}
+
+// The CTA whose share [range_start(c), range_start(c + 1)) holds unit x.
+__device__ __forceinline__ int range_owner(int x, int W, int grid) {
+  return (int)(((unsigned long long)(x + 1) * (unsigned)grid - 1ull) / (unsigned)W);
 }
 
 // Decode-step cache write of sequence b, vectors first, first + stride, ...:
@@ -222,61 +243,128 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
   allow_next_grid();
   wait_prior_grid();           // inputs may come from the previous kernel in the stream
   if (warp >= 2) {
-    // tile prefix over the batch (every CTA computes it; CTA 0 also stores it for
-    // the combine pass), zero rows of empty sequences, length checks
+    // The split (every CTA computes it; CTA 0 also stores the prefixes for the
+    // combine pass), zero rows of empty sequences, length checks.  Thread et
+    // walks the sequences [b0, b1) three times: totals, then prefixes and the
+    // CTA's cuts, then its window entries.
     const int et = threadIdx.x - 64, ew = et >> 5;
     const int per = (p.B + 127) / 128;
     const int b0 = min(p.B, et * per), b1 = min(p.B, b0 + per);
-    int mine = 0;
-    for (int b = b0; b < b1; ++b) mine += (clamp_len(p, b) + TT - 1) / TT;
-    int inc = mine;
+    int my_t = 0, my_n = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int nt = (clamp_len(p, b) + TT - 1) / TT;
+      my_t += nt;
+      my_n += nt > 0;
+    }
+    int inc_t = my_t, inc_n = my_n;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-      if (lane >= o) inc += v;
+      const int vt = __shfl_up_sync(0xFFFFFFFFu, inc_t, o);
+      const int vn = __shfl_up_sync(0xFFFFFFFFu, inc_n, o);
+      if (lane >= o) {
+        inc_t += vt;
+        inc_n += vn;
+      }
     }
-    if (lane == 31) tl->scan[ew] = inc;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    int before = 0;
-    for (int w = 0; w < ew; ++w) before += tl->scan[w];
-    int run = before + inc - mine;
+    if (lane == 31) {
+      tl->scan[0][ew] = inc_t;
+      tl->scan[1][ew] = inc_n;
+    }
+    named_barrier(1, 128);
+    int run_t = inc_t - my_t, run_n = inc_n - my_n, T = 0, NE = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      if (w < ew) {
+        run_t += tl->scan[0][w];
+        run_n += tl->scan[1][w];
+      }
+      T += tl->scan[0][w];
+      NE += tl->scan[1][w];
+    }
+    const int W = T + kStartWeight * NE;
+    const int x0 = range_start(c, W, grid), x1 = range_start(c + 1, W, grid);
+    const int first_t = run_t, first_n = run_n;
     for (int b = b0; b < b1; ++b) {
-      tl->prefix[b] = run;
-      if (c == 0) sp.tile_prefix[b] = run;
       const int raw = p.seq_lens[b];
       const int L = clamp_len(p, b);
-      if (c == 0 && (raw < 0 || raw > p.max_seq_len)) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+      const int nt = (L + TT - 1) / TT;
+      const int run_w = run_t + kStartWeight * run_n;
+      if (c == 0) {
+        sp.tile_prefix[b] = run_t;
+        sp.weight_prefix[b] = run_w;
+        if (raw < 0 || raw > p.max_seq_len) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+      }
       if (L == 0 && b % grid == c) {
         uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)b * p.Hq * kD;
         for (int e = 0; e < p.Hq * kD; ++e) o[e] = 0;
         if (p.new_k != nullptr) store_newest<H>(p, b, 0, 1);   // no tile reads it
       }
-      run += (L + TT - 1) / TT;
+      if (nt > 0) {
+        // weighted span [run_w, run_w + kStartWeight + nt): the start, then the
+        // tiles; a cut in it falls before tile clamp(x - run_w - start, 0, nt)
+        const int span_end = run_w + kStartWeight + nt;
+        if (run_w <= x0 && x0 < span_end) {
+          const int tb = run_t + min(max(x0 - run_w - kStartWeight, 0), nt);
+          tl->cut[0] = tb;
+          // the window starts at the sequence holding tile tb (this one, or,
+          // when the cut is at its end, the next non-empty one)
+          tl->win_n[0] = tb < run_t + nt ? run_n : run_n + 1;
+        }
+        if (run_w <= x1 && x1 < span_end) {
+          const int te = run_t + min(max(x1 - run_w - kStartWeight, 0), nt);
+          tl->cut[1] = te;
+          tl->win_n[1] = te > run_t ? run_n + 1 : run_n;   // sequences before the end cut
+        }
+      }
+      run_t += nt;
+      run_n += nt > 0;
     }
     if (et == 127) {
-      tl->prefix[p.B] = run;
-      if (c == 0) sp.tile_prefix[p.B] = run;
+      if (c == 0) {
+        sp.tile_prefix[p.B] = run_t;
+        sp.weight_prefix[p.B] = run_t + kStartWeight * run_n;
+      }
+      if (x0 >= W) {              // cuts at the batch's end (or an empty batch)
+        tl->cut[0] = T;
+        tl->win_n[0] = NE;
+      }
+      if (x1 >= W) {
+        tl->cut[1] = T;
+        tl->win_n[1] = NE;
+      }
     }
+    named_barrier(1, 128);
+    const int wn0 = tl->win_n[0], wn1 = tl->cut[0] < tl->cut[1] ? tl->win_n[1] : wn0;
+    run_t = first_t;
+    run_n = first_n;
+    for (int b = b0; b < b1; ++b) {
+      const int nt = (clamp_len(p, b) + TT - 1) / TT;
+      if (nt > 0 && run_n >= wn0 && run_n < wn1) {
+        const int k = run_n - wn0;          // < kWin: the host bounds B by kWin * grid
+        if (k < kWin) {
+          tl->win_b[k] = b;
+          tl->win_tp[k] = run_t;
+          if (run_n == wn1 - 1) tl->win_tp[k + 1] = run_t + nt;
+        }
+      }
+      run_t += nt;
+      run_n += nt > 0;
+    }
+    if (et == 0) tl->nwin = min(wn1 - wn0, kWin);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int T = tl->prefix[p.B];
-  const int t_begin = range_start(c, T, grid), t_end = range_start(c + 1, T, grid);
+  const int t_begin = tl->cut[0], t_end = tl->nwin > 0 ? tl->cut[1] : tl->cut[0];
+  const int nwin = tl->nwin;
   if (warp >= 2) {
     // Decode-step cache write: the newest token of a sequence lies in its last
     // tile, and tiles cover disjoint token ranges, so the CTA whose range holds
     // that tile stores the token.  The writes are fenced against the async
     // proxy; the producer waits for app_done before it loads such a tile.
-    if (p.new_k != nullptr && t_begin < t_end) {
-      int lo = 0, hi = p.B;            // first sequence whose last tile is >= t_begin
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (tl->prefix[mid + 1] > t_begin) hi = mid;
-        else lo = mid + 1;
-      }
-      for (int b = lo; b < p.B && tl->prefix[b + 1] <= t_end; ++b)
-        if (tl->prefix[b + 1] > tl->prefix[b]) store_newest<H>(p, b, threadIdx.x - 64, 128);
+    if (p.new_k != nullptr) {
+      for (int k = 0; k < nwin && tl->win_tp[k + 1] <= t_end; ++k)
+        store_newest<H>(p, tl->win_b[k], threadIdx.x - 64, 128);
     }
     fence_async_global();
     mbar_arrive(&tl->app_done);
@@ -353,35 +441,21 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     // (~4 us under load on GB300) held up the first S of every segment.
     int next_b = -1;                   // sequence of the next segment, -1: none
     bool q_early = false;              // the next segment's Q is already on its way
-    int b = 0;
-    if (t_begin < t_end) {        // the sequence holding this CTA's first tile
-      int lo = 0, hi = p.B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tl->prefix[mid] <= t_begin) lo = mid;
-        else hi = mid - 1;
-      }
-      b = lo;
-    }
+    int wk = 0;                        // window entry of the next segment
+    int tpb = 0, tpb1 = 0;             // batch tiles of the segment's sequence
     while (ok) {
       SegInfo sg;
       sg.valid = 0;
-      int tpb = 0;
       if (tile < t_end) {
-        int tpb1;
-        for (;;) {                       // skip sequences without tiles
-          tpb = tl->prefix[b];
-          tpb1 = tl->prefix[b + 1];
-          if (tpb1 > tile) break;
-          ++b;
-        }
-        sg.b = b;
-        if (pf_b != b) {                 // first segment: nothing prefetched
-          pf_b = b;
-          pf_len = p.seq_lens[b];
+        tpb = tl->win_tp[wk];
+        tpb1 = tl->win_tp[wk + 1];
+        sg.b = tl->win_b[wk];
+        if (pf_b != sg.b) {              // first segment: nothing prefetched
+          pf_b = sg.b;
+          pf_len = p.seq_lens[sg.b];
           const int kf = ((tile - tpb) * TT) / p.bs;
-          pf_cur = raw_ids(b, kf);
-          pf_nxt = raw_ids(b, kf + 32);
+          pf_cur = raw_ids(sg.b, kf);
+          pf_nxt = raw_ids(sg.b, kf + 32);
         }
         sg.L = pf_len < 0 ? 0 : (pf_len > p.max_seq_len ? p.max_seq_len : pf_len);
         sg.j0 = tile - tpb;
@@ -429,11 +503,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       const int nblk_seq = (sg.L + p.bs - 1) / p.bs;
       int kb = (sg.j0 * TT) / p.bs;
       int32_t cur = pf_cur, nxt = pf_nxt;
-      const int seq_tiles = tl->prefix[sg.b + 1] - tl->prefix[sg.b];
+      const int seq_tiles = tpb1 - tpb;
       next_b = -1;
-      if (tl->prefix[sg.b] + sg.j1 < t_end) {   // the next segment: the next sequence with tiles
-        int nb = sg.b + 1;
-        while (tl->prefix[nb + 1] == tl->prefix[nb]) ++nb;
+      if (tpb + sg.j1 < t_end) {       // the next segment: the next window entry
+        const int nb = tl->win_b[wk + 1];
         next_b = nb;
         pf_b = nb;
         pf_len = p.seq_lens[nb];
@@ -509,7 +582,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       if (!ok) break;
       tile = tpb + sg.j1;
-      ++b;
+      ++wk;
       ++seg_idx;
       __syncwarp();
     }
@@ -910,8 +983,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
 }
 
 // Merge the partials of sequences cut by CTA range boundaries.  One warp per
-// (sequence, query head): lane i reads part i's (max, sum) once, then the
-// accumulators are summed with the per-part weights, eight loads in flight.
+// (sequence, query head).  Two rounds of loads: the sequence's prefixes, then,
+// all at once, every part's (max, sum) (lane i: part i) and the first eight
+// parts' accumulators (each lane its four columns); parts past the eighth are
+// read afterwards, eight in flight.
 // No early launch of the next kernel: letting the next decode's CTAs become
 // resident while this grid runs measured 3% slower on the long-context batch
 // on GB300 (and no faster on the others).
@@ -920,53 +995,72 @@ __global__ void __launch_bounds__(128)
 combine_sk_kernel(const SkParams sp, int grid) {
   const DecodeParams& p = sp.p;
   constexpr int PER = kD / 32;
+  constexpr int kEarly = 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  wait_prior_grid();           // partials and the tile prefix come from the main kernel
+  wait_prior_grid();           // partials and the prefixes come from the main kernel
   const int64_t row = (int64_t)blockIdx.x * 4 + warp;
   if (row >= (int64_t)p.B * p.Hq) return;
   const int b = (int)(row / p.Hq), q = (int)(row - (int64_t)b * p.Hq);
-  const int T = sp.tile_prefix[p.B];
+  const int W = sp.weight_prefix[p.B];
   const int tpb = sp.tile_prefix[b], tpb1 = sp.tile_prefix[b + 1];
+  const int pwb = sp.weight_prefix[b];
   if (tpb1 <= tpb) return;                                  // empty: zeroed by the main kernel
-  auto owner = [&](int x) { return (int)(((unsigned)(x + 1) * (unsigned)grid - 1u) / (unsigned)T); };
-  const int cf = owner(tpb), cl = owner(tpb1 - 1);
+  // weighted position of the sequence's tile j: pwb + kStartWeight + j
+  const int cf = range_owner(pwb + kStartWeight, W, grid);
+  const int cl = range_owner(pwb + kStartWeight + (tpb1 - tpb) - 1, W, grid);
   if (cf == cl) return;                                     // written directly
   const int nparts = cl - cf + 1;
-  // per-lane part: its partial index (or -1 for a CTA whose range is empty)
+  // part i: CTA cf + i, slot 0 when the sequence is that CTA's first segment
+  // (every CTA after cf; cf when its range starts at or after the sequence's
+  // start), else 1; -1 for a CTA with an empty range
   auto part_index = [&](int i) -> int64_t {
     const int cc = cf + i;
-    const int st = range_start(cc, T, grid);
-    if (st == range_start(cc + 1, T, grid)) return -1;
-    const int slot = st >= tpb ? 0 : 1;
+    const int st = range_start(cc, W, grid);
+    if (st == range_start(cc + 1, W, grid)) return -1;
+    const int slot = (cc > cf || st >= pwb) ? 0 : 1;
     return ((int64_t)cc * 2 + slot) * p.Hq + q;
   };
-  // the first 32 parts' (max, sum) stay in registers; more parts are read again
-  float M = -CUDART_INF_F, m0 = -CUDART_INF_F, l0 = 0.f;
   const int64_t idx0 = lane < nparts ? part_index(lane) : -1;
+  float m0 = -CUDART_INF_F, l0 = 0.f;
   if (idx0 >= 0) {
     m0 = sp.part_m[idx0];
     l0 = sp.part_l[idx0];
-    M = m0;
   }
+  float4 early[kEarly];
+#pragma unroll
+  for (int k = 0; k < kEarly; ++k) {
+    const long long ik = __shfl_sync(0xFFFFFFFFu, (long long)idx0, k);
+    early[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k < nparts && ik >= 0)
+      early[k] = *reinterpret_cast<const float4*>(sp.part_acc + ik * kD + lane * PER);
+  }
+  // the first 32 parts' (max, sum) stay in registers; more parts are read again
+  float M = m0;
   for (int i = lane + 32; i < nparts; i += 32) {
     const int64_t idx = part_index(i);
     if (idx >= 0) M = fmaxf(M, sp.part_m[idx]);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-  float den = 0.f, acc[PER];
+  const float w0 = idx0 >= 0 ? exp2f(m0 - M) : 0.f;
+  float den = w0 * l0, acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int k = 0; k < kEarly; ++k) {
+    const float wk = __shfl_sync(0xFFFFFFFFu, w0, k);      // 0 for missing parts
+    acc[0] = fmaf(wk, early[k].x, acc[0]);
+    acc[1] = fmaf(wk, early[k].y, acc[1]);
+    acc[2] = fmaf(wk, early[k].z, acc[2]);
+    acc[3] = fmaf(wk, early[k].w, acc[3]);
+  }
   for (int base = 0; base < nparts; base += 32) {
     const int i = base + lane;
     int64_t idx = -1;
     float w = 0.f;
     if (base == 0) {
       idx = idx0;
-      if (idx >= 0) {
-        w = exp2f(m0 - M);
-        den = fmaf(w, l0, den);
-      }
+      w = w0;
     } else if (i < nparts) {
       idx = part_index(i);
       if (idx >= 0) {
@@ -976,7 +1070,7 @@ combine_sk_kernel(const SkParams sp, int grid) {
     }
     const int cnt = min(32, nparts - base);
 #pragma unroll 8
-    for (int k = 0; k < cnt; ++k) {
+    for (int k = base == 0 ? kEarly : 0; k < cnt; ++k) {
       const float wk = __shfl_sync(0xFFFFFFFFu, w, k);
       const long long ik = __shfl_sync(0xFFFFFFFFu, (long long)idx, k);
       if (ik >= 0) {
@@ -1093,6 +1187,12 @@ bool tcg_supported(const DecodeParams& p) {
   // a bad block id is redirected to row num_blocks * bs (+ offset < 64): stays an int
   if ((long long)p.num_blocks * p.bs + 64 >= (1ll << 31)) return false;
   if ((long long)p.B * p.Hq >= (1ll << 31)) return false;
+  // the batch's weight (tiles + one per sequence) stays an int
+  const long long TT = kRows / p.Hkv;
+  if ((long long)p.B * ((p.max_seq_len + TT - 1) / TT + kStartWeight) >= (1ll << 31)) return false;
+  // a CTA's range meets at most B / grid + 2 sequences: they fit its window
+  const int grid = device_sms() < kSkMaxGrid ? device_sms() : kSkMaxGrid;
+  if (grid <= 0 || (long long)p.B > (long long)(kWin - 2) * grid) return false;
   return encode_fn() != nullptr;
 }
 
@@ -1100,7 +1200,8 @@ SkLayout sk_layout(int B, int Hq) {
   auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
   SkLayout l;
   l.prefix_off = 0;
-  l.m_off = l.prefix_off + a((size_t)(B + 1) * sizeof(int));
+  l.wprefix_off = l.prefix_off + a((size_t)(B + 1) * sizeof(int));
+  l.m_off = l.wprefix_off + a((size_t)(B + 1) * sizeof(int));
   const size_t parts = (size_t)kSkMaxGrid * 2 * Hq;
   l.l_off = l.m_off + a(parts * sizeof(float));
   l.acc_off = l.l_off + a(parts * sizeof(float));
@@ -1150,6 +1251,7 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
   SkParams sp;
   sp.p = p;
   sp.tile_prefix = reinterpret_cast<int*>(ws + l.prefix_off);
+  sp.weight_prefix = reinterpret_cast<int*>(ws + l.wprefix_off);
   sp.part_m = reinterpret_cast<float*>(ws + l.m_off);
   sp.part_l = reinterpret_cast<float*>(ws + l.l_off);
   sp.part_acc = reinterpret_cast<float*>(ws + l.acc_off);
@@ -1161,6 +1263,17 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
   const long long rows = (long long)p.B * p.Hq;
   if (rows == 0) return PA_OK;
   const int cgrid = (int)((rows + 3) / 4);
+  // The combine keeps the main kernel's shared-memory carve-out, so an SM does
+  // not switch L1 / shared-memory configuration between the two kernels.
+  static std::once_flag carve_once;
+  std::call_once(carve_once, [] {
+    cudaFuncSetAttribute(combine_sk_kernel<PA_BFLOAT16>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(combine_sk_kernel<PA_FLOAT16>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+  });
   const cudaError_t e =
       p.dtype == PA_BFLOAT16
           ? launch_pdl(combine_sk_kernel<PA_BFLOAT16>, dim3((unsigned)cgrid), 128, 0, stream, sp, grid)

@@ -52,10 +52,11 @@ bool tc_supported(const DecodeParams& p);
 pa_status launch_decode_tc(const DecodeParams& p, int2* items, int* queue, cudaStream_t stream);
 
 // Tensor-core path, all KV heads of a block per CTA with a stream-K split
-// (head_dim 128, Hkv in {1,2,4,8,16,32}, G in {1,2,4,8}, Hq <= 64): main + combine.
+// (head_dim 128, Hkv in {1,2,4,8,16,32}, G in {1,2,4,8}, Hq <= 64, up to
+// 16384 sequences): main + combine.
 constexpr int kSkMaxGrid = 160;          // persistent CTAs at most (GB300: 152 SMs)
 struct SkLayout {
-  size_t prefix_off, m_off, l_off, acc_off, total;
+  size_t prefix_off, wprefix_off, m_off, l_off, acc_off, total;
 };
 SkLayout sk_layout(int B, int Hq);
 bool tcg_supported(const DecodeParams& p);

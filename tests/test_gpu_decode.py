@@ -276,14 +276,21 @@ def test_one_workspace_serves_a_sequence_of_batches(pa):
     assert torch.equal(outs[0].view(torch.int16), outs[3].view(torch.int16))
 
 
-def test_more_sequences_than_the_grouped_kernel_serves(pa):
-    """1,100 short sequences: past the grouped kernel's 1,023-sequence limit, the
-    call takes another kernel and stays exact within the tolerance."""
-    w = _small("llama3_8b", num_seqs=1100, length_kind="uniform", lo=1, hi=300, seed=77)
+@pytest.mark.parametrize("B,hi", [(1100, 300), (4000, 64)])
+def test_large_batches(pa, B, hi):
+    """Thousands of short sequences (continuous batching with many live
+    requests): the grouped kernel serves them (each CTA's range meets dozens of
+    sequences, most of them whole); checked on sampled rows and on every row of
+    the sequences around CTA range boundaries' typical spacing."""
+    w = _small("llama3_8b", num_seqs=B, length_kind="uniform", lo=1, hi=hi, seed=77 + B)
     batch = scenarios.fixed_batch(w, fill_all=True)
-    got = widen(DeviceBatch(batch).decode(pa))
-    rows = list(range(0, 1100, 37)) + [1099]
-    assert_close(got[rows], scenarios.decode_f64(batch, sequences=rows)[rows], "B=1100")
+    dev = DeviceBatch(batch)
+    if pa.decode_path == "tc":
+        assert pa.decode_kernel_for(dev.q, dev.k_pool, dev.tables,
+                                    int(batch.seq_lens.max())) == "grouped"
+    got = widen(dev.decode(pa))
+    rows = sorted(set(list(range(0, B, 37)) + list(range(B // 2, B // 2 + 40)) + [B - 1]))
+    assert_close(got[rows], scenarios.decode_f64(batch, sequences=rows)[rows], f"B={B}")
 
 
 @pytest.mark.parametrize("hq,hkv,bs", [(32, 32, 16), (32, 32, 8), (8, 1, 32), (64, 16, 64)])
@@ -298,8 +305,8 @@ def test_more_kv_heads_per_block_ragged(pa, hq, hkv, bs):
 
 
 def test_workspace_of_exactly_the_grouped_kernels_size(pa):
-    """The grouped kernel's workspace is its stream-K area only (tile prefix,
-    per-CTA (max, sum) and accumulators of up to 160 CTAs x 2 segments), whatever
+    """The grouped kernel's workspace is its stream-K area only (tile and weight
+    prefixes, per-CTA (max, sum) and accumulators of up to 160 CTAs x 2 segments), whatever
     the lengths: pa_decode runs with exactly that many bytes and refuses one
     fewer; the result matches the oracle."""
     if pa.decode_path != "tc":
@@ -313,7 +320,7 @@ def test_workspace_of_exactly_the_grouped_kernels_size(pa):
     n = pa.pa_decode_workspace_bytes_for(B, Hq, w.num_kv_heads, D, w.block_size,
                                          dev.tables.shape[1], batch.num_blocks, max_len, 1)
     parts = 160 * 2 * Hq
-    assert n == (-(-4 * (B + 1) // 256) * 256) + 2 * (-(-4 * parts // 256) * 256) + \
+    assert n == 2 * (-(-4 * (B + 1) // 256) * 256) + 2 * (-(-4 * parts // 256) * 256) + \
         (-(-4 * parts * D // 256) * 256)
     ws = torch.empty(n, dtype=torch.uint8, device="cuda")
     out = torch.empty_like(dev.q)
