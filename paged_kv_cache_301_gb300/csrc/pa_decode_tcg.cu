@@ -56,7 +56,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 232448 - 1024;   // per-block limit minus alignment slack
 constexpr int kStartWeight = 1;              // a sequence start weighs one tile in the split
-constexpr int kWin = 1024;                   // sequences of one CTA's range (shared memory)
+constexpr int kWin = 640;                    // sequences of one CTA's range (shared memory)
 constexpr int kMaxSeqs = 16384;              // batch size served: B / grid + 2 <= kWin
 
 
@@ -88,6 +88,7 @@ struct Tail {
   // batch order.  Entry k is sequence win_b[k], whose tiles are the batch tiles
   // [win_tp[k], win_tp[k+1]).
   int win_b[kWin];
+  int win_len[kWin];          // its length (clamped to [0, max_seq_len])
   int win_tp[kWin + 1];
   int nwin;
   int cut[2];                 // the CTA's tile range [cut[0], cut[1])
@@ -306,9 +307,14 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (run_w <= x0 && x0 < span_end) {
           const int tb = run_t + min(max(x0 - run_w - kStartWeight, 0), nt);
           tl->cut[0] = tb;
-          // the window starts at the sequence holding tile tb (this one, or,
-          // when the cut is at its end, the next non-empty one)
-          tl->win_n[0] = tb < run_t + nt ? run_n : run_n + 1;
+          // the window starts at the sequence holding tile tb (tb < run_t + nt
+          // here); its first block ids go to L2 now, so that the producer's
+          // first load of them does not wait for DRAM
+          tl->win_n[0] = run_n;
+          const int kf = (tb - run_t) * TT / p.bs;
+          const int32_t* ids = p.block_tables + (int64_t)b * p.max_blocks + kf;
+          prefetch_l2(ids);
+          if (kf + 32 < p.max_blocks) prefetch_l2(ids + 32);
         }
         if (run_w <= x1 && x1 < span_end) {
           const int te = run_t + min(max(x1 - run_w - kStartWeight, 0), nt);
@@ -343,6 +349,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int k = run_n - wn0;          // < kWin: the host bounds B by kWin * grid
         if (k < kWin) {
           tl->win_b[k] = b;
+          tl->win_len[k] = clamp_len(p, b);
           tl->win_tp[k] = run_t;
           if (run_n == wn1 - 1) tl->win_tp[k + 1] = run_t + nt;
         }
@@ -433,7 +440,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       const int k = base + lane;
       return k < p.max_blocks ? p.block_tables[(int64_t)bb * p.max_blocks + k] : 0;
     };
-    int pf_b = -1, pf_len = 0;
+    int pf_b = -1;
     int32_t pf_cur = 0, pf_nxt = 0;
     // With two Q buffers the next segment's Q is copied as soon as its buffer is
     // free (polled once per tile, never waited on), instead of at the segment's
@@ -452,12 +459,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         sg.b = tl->win_b[wk];
         if (pf_b != sg.b) {              // first segment: nothing prefetched
           pf_b = sg.b;
-          pf_len = p.seq_lens[sg.b];
           const int kf = ((tile - tpb) * TT) / p.bs;
           pf_cur = raw_ids(sg.b, kf);
           pf_nxt = raw_ids(sg.b, kf + 32);
         }
-        sg.L = pf_len < 0 ? 0 : (pf_len > p.max_seq_len ? p.max_seq_len : pf_len);
+        sg.L = tl->win_len[wk];
         sg.j0 = tile - tpb;
         sg.j1 = min(t_end, tpb1) - tpb;
         sg.direct = (sg.j0 == 0 && sg.j1 == tpb1 - tpb);
@@ -509,7 +515,6 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int nb = tl->win_b[wk + 1];
         next_b = nb;
         pf_b = nb;
-        pf_len = p.seq_lens[nb];
         pf_cur = raw_ids(nb, 0);
         pf_nxt = raw_ids(nb, 32);
       }
