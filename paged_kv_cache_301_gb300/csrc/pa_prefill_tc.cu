@@ -107,10 +107,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
   allow_next_grid();
   wait_prior_grid();               // q, the pools and the tables may come from the previous kernel
-  // blockIdx.x walks the query-tile pairs of one (sequence, KV head), longest
-  // causal work first, so the CTAs resident together read the same K/V from L2
-  const int b = blockIdx.y / p.Hkv, h = blockIdx.y - b * p.Hkv;
-  const int qp = p.n_qpairs - 1 - (int)blockIdx.x;
+  // blockIdx.x walks the (sequence, KV head) pairs and blockIdx.y the query-tile
+  // pairs, longest causal work first: CTAs resident together read different
+  // K/V, and each (sequence, KV head)'s K/V stays in L2 for its later query tiles
+  const int b = blockIdx.x / p.Hkv, h = blockIdx.x - b * p.Hkv;
+  const int qp = p.n_qpairs - 1 - (int)blockIdx.y;
   const int qs = p.q_start[b];
   const int n = p.q_start[b + 1] - qs;
   const int L = p.seq_lens[b];
@@ -395,12 +396,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
             ls += pa_ + pb_;
             if (DT == PA_BFLOAT16) {
-              // hi = the top 16 bits (truncation), lo = the rest rounded: hi + lo
-              // carries ~16 significant bits either way
+              // hi = the top 16 bits (truncation), lo = the remainder, truncated
+              // too: hi + lo carries ~15 significant bits with byte permutes
+              // only (no conversion instruction)
               const uint32_t ua = __float_as_uint(pa_), ub = __float_as_uint(pb_);
               pw[e >> 1] = __byte_perm(ua, ub, 0x7632);
-              pw[8 + (e >> 1)] = narrow2<DT>(pa_ - __uint_as_float(ua & 0xFFFF0000u),
-                                             pb_ - __uint_as_float(ub & 0xFFFF0000u));
+              pw[8 + (e >> 1)] =
+                  __byte_perm(__float_as_uint(pa_ - __uint_as_float(ua & 0xFFFF0000u)),
+                              __float_as_uint(pb_ - __uint_as_float(ub & 0xFFFF0000u)), 0x7632);
             } else {
               const uint32_t h2 = narrow2<DT>(pa_, pb_);
               const float2 hf = widen2<DT>(h2);
@@ -408,7 +411,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
               pw[8 + (e >> 1)] = narrow2<DT>(pa_ - hf.x, pb_ - hf.y);
             }
           }
-          tmem_st16(scol + c0 + g, pw);          // over S columns already read
+          tmem_st16_nowait(scol + c0 + g, pw);   // over S columns already read
         }
       }
       // Rows that raised their max rescale O (complete up to tile t-1, P.V(t) not
@@ -445,6 +448,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       // consume P.V(t-1)'s completion before P(t) is released, so the barrier
       // cannot run two phases ahead of any waiting warp
       if (t > 0 && !wait_all(&tl->pv_done[k], (t - 1) & 1)) { ok = false; break; }
+      tmem_wait_st();                            // every P word is in tensor memory
       tc_fence_before();
       fence_async_smem();
       __syncwarp();
@@ -520,7 +524,7 @@ pa_status launch_g(const PrefillParams& p, const CUtensorMap& k, const CUtensorM
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr != cudaSuccess) return PA_ERR_CUDA;
-  const dim3 grid((unsigned)p.n_qpairs, (unsigned)(p.Hkv * p.B));
+  const dim3 grid((unsigned)(p.Hkv * p.B), (unsigned)p.n_qpairs);
   if (launch_pdl(prefill_tc_kernel<DT, G>, grid, kThreads, kSmemBytes, stream, k, v, q, p) !=
       cudaSuccess)
     return PA_ERR_CUDA;
@@ -607,7 +611,8 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
   }
   const int TQ = kRows / G;
   const int64_t n_qtiles = ((int64_t)max_q_len + TQ - 1) / TQ;
-  if ((int64_t)num_seqs * num_kv_heads > 65535) return PA_ERR_INVALID_ARG;   // grid y
+  if ((n_qtiles + 1) / 2 > 65535 || (int64_t)num_seqs * num_kv_heads > 0x7FFFFFFF)
+    return PA_ERR_INVALID_ARG;                                              // grid y, x
 
   const CUtensorMapDataType dt =
       dtype == PA_BFLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
