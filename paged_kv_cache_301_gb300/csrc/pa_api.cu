@@ -14,9 +14,9 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 WorkspaceLayout workspace_layout(DecodeKernel k, int B, int Hq, int D, int P) {
   const size_t rows = (size_t)B * Hq * P;
   WorkspaceLayout w = {};
-  if (k == DecodeKernel::kGrouped) {
+  if (k == DecodeKernel::kGrouped) {      // per pass: at most kMaxHq query heads
     w.sk_off = 0;
-    w.total = sk_layout(B, Hq).total;
+    w.total = sk_layout(B, Hq < 64 ? Hq : 64).total;
     return w;
   }
   size_t off = 0;
@@ -113,6 +113,9 @@ static pa_status check_shape(int num_seqs, int num_q_heads, int num_kv_heads, in
   p->dtype = dtype;
   p->PT = pt;
   p->P = max(1, num_partitions(max_seq_len, pt));
+  p->Hkv_all = num_kv_heads;
+  p->Hq_all = num_q_heads;
+  p->head_off = 0;
   return PA_OK;
 }
 

@@ -159,7 +159,8 @@ __device__ __forceinline__ int range_owner(int x, int W, int grid) {
 // reports it); a block id outside the pool is reported and skipped.
 template <int H>
 __device__ __forceinline__ void store_newest(const DecodeParams& p, int b, int first, int stride) {
-  constexpr int kRowVecs = H * kD * 2 / 16;
+  constexpr int kRowVecs = H * kD * 2 / 16;     // this launch's heads of a token
+  const int64_t all_vecs = (int64_t)p.Hkv_all * kD * 2 / 16, off_vecs = (int64_t)p.head_off * kD * 2 / 16;
   const int L = p.seq_lens[b];
   if (L <= 0 || L > p.max_blocks * p.bs) return;
   const int pos = L - 1;
@@ -168,9 +169,9 @@ __device__ __forceinline__ void store_newest(const DecodeParams& p, int b, int f
     if (first == 0) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
     return;
   }
-  const int64_t dst = ((int64_t)id * p.bs + pos % p.bs) * kRowVecs;
-  const uint4* sk = static_cast<const uint4*>(p.new_k) + (int64_t)b * kRowVecs;
-  const uint4* sv = static_cast<const uint4*>(p.new_v) + (int64_t)b * kRowVecs;
+  const int64_t dst = ((int64_t)id * p.bs + pos % p.bs) * all_vecs + off_vecs;
+  const uint4* sk = static_cast<const uint4*>(p.new_k) + (int64_t)b * all_vecs + off_vecs;
+  const uint4* sv = static_cast<const uint4*>(p.new_v) + (int64_t)b * all_vecs + off_vecs;
   uint4* dk = static_cast<uint4*>(const_cast<void*>(p.k_pool)) + dst;
   uint4* dv = static_cast<uint4*>(const_cast<void*>(p.v_pool)) + dst;
   for (int v = first; v < kRowVecs; v += stride) {
@@ -296,7 +297,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (raw < 0 || raw > p.max_seq_len) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
       }
       if (L == 0 && b % grid == c) {
-        uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)b * p.Hq * kD;
+        uint16_t* o = static_cast<uint16_t*>(p.out) + ((int64_t)b * p.Hq_all + p.head_off * G) * kD;
         for (int e = 0; e < p.Hq * kD; ++e) o[e] = 0;
         if (p.new_k != nullptr) store_newest<H>(p, b, 0, 1);   // no tile reads it
       }
@@ -496,9 +497,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         ok = mbar_wait(&tl->q_empty[qb], qph ^ 1, abort_flag, kWaitNs);
         if (ok) {
           mbar_arrive_expect_tx(&tl->q_full[qb], Gm::kQBytes);
-          tma_load_2d(smem + Gm::kQOff + qb * Gm::kQBytes, &tm_q, &tl->q_full[qb], 0, sg.b * p.Hq);
+          tma_load_2d(smem + Gm::kQOff + qb * Gm::kQBytes, &tm_q, &tl->q_full[qb], 0,
+                      sg.b * p.Hq_all + p.head_off * G);
           tma_load_2d(smem + Gm::kQOff + qb * Gm::kQBytes + N * 128, &tm_q, &tl->q_full[qb], 64,
-                      sg.b * p.Hq);
+                      sg.b * p.Hq_all + p.head_off * G);
           q_issued[qb] = qph;
         } else {
           set_abort();
@@ -571,9 +573,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
           if (lane == 0 && mbar_try_wait(&tl->q_empty[nqb], nqph ^ 1)) {
             mbar_arrive_expect_tx(&tl->q_full[nqb], Gm::kQBytes);
             tma_load_2d(smem + Gm::kQOff + nqb * Gm::kQBytes, &tm_q, &tl->q_full[nqb], 0,
-                        next_b * p.Hq);
+                        next_b * p.Hq_all + p.head_off * G);
             tma_load_2d(smem + Gm::kQOff + nqb * Gm::kQBytes + N * 128, &tm_q, &tl->q_full[nqb],
-                        64, next_b * p.Hq);
+                        64, next_b * p.Hq_all + p.head_off * G);
             q_issued[nqb] = nqph;
             go = 1;
           }
@@ -925,7 +927,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
           sp.part_l[part0 + q] = tl->lred[0][q] + tl->lred[1][q] + tl->lred[2][q] + tl->lred[3][q];
         }
       }
-      const int64_t out0 = sg.direct ? (int64_t)sg.b * Hq * kD : part0 * kD;
+      const int64_t out0 =
+          sg.direct ? ((int64_t)sg.b * p.Hq_all + p.head_off * G) * kD : part0 * kD;
       const int last_ps = (tile_g + ntiles - 1) % Gm::kPBufs;
       if (sg.last || kStageP) {
         // final segment: every MMA has completed and every copy has landed, the
@@ -1090,7 +1093,8 @@ combine_sk_kernel(const SkParams sp, int grid) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
   const float inv = 1.f / den;
-  uint16_t* out = static_cast<uint16_t*>(p.out) + row * kD + lane * PER;
+  const int64_t orow = (int64_t)b * p.Hq_all + (int64_t)p.head_off * (p.Hq / p.Hkv) + q;
+  uint16_t* out = static_cast<uint16_t*>(p.out) + orow * kD + lane * PER;
   uint2 packed;
   packed.x = narrow2<DT>(acc[0] * inv, acc[1] * inv);
   packed.y = narrow2<DT>(acc[2] * inv, acc[3] * inv);
@@ -1160,6 +1164,7 @@ pa_status launch_h(int G, const SkParams& sp, const CUtensorMap& k, const CUtens
     case 2: return launch_hg<DT, H, 2>(sp, k, v, q, grid, stream);
     case 4: return launch_hg<DT, H, 4>(sp, k, v, q, grid, stream);
     case 8: return launch_hg<DT, H, 8>(sp, k, v, q, grid, stream);
+    case 16: return launch_hg<DT, H, 16>(sp, k, v, q, grid, stream);
     default: return PA_ERR_UNSUPPORTED;
   }
 }
@@ -1181,19 +1186,28 @@ pa_status launch_dt(int H, int G, const SkParams& sp, const CUtensorMap& k, cons
 
 }  // namespace
 
+// KV heads per pass: all of them when their query heads fit one pass (thread d
+// of the softmax warps keeps one accumulator per query head, at most kMaxHq),
+// else the largest group of 1, 2, 4, 8, 16 or 32 heads that divides Hkv and
+// whose query heads fit; 0 when none does.
+int heads_per_pass(int Hkv, int G) {
+  for (int hg = 32; hg >= 1; hg >>= 1)
+    if (hg <= Hkv && Hkv % hg == 0 && hg * G <= kMaxHq) return hg;
+  return 0;
+}
+
 bool tcg_supported(const DecodeParams& p) {
   const int G = p.Hq / p.Hkv;
   if (p.D != kD) return false;
-  if (p.Hkv != 1 && p.Hkv != 2 && p.Hkv != 4 && p.Hkv != 8 && p.Hkv != 16 && p.Hkv != 32)
-    return false;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return false;
+  const int hg = heads_per_pass(p.Hkv, G);
+  if (hg == 0) return false;
   if (p.B > kMaxSeqs) return false;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return false;
-  if (p.Hq > kMaxHq) return false;
   // a bad block id is redirected to row num_blocks * bs (+ offset < 64): stays an int
   if ((long long)p.num_blocks * p.bs + 64 >= (1ll << 31)) return false;
   if ((long long)p.B * p.Hq >= (1ll << 31)) return false;
   // the batch's weight (tiles + one per sequence) stays an int
-  const long long TT = kRows / p.Hkv;
+  const long long TT = kRows / hg;
   if ((long long)p.B * ((p.max_seq_len + TT - 1) / TT + kStartWeight) >= (1ll << 31)) return false;
   // a CTA's range meets at most B / grid + 2 sequences: they fit its window
   const int grid = device_sms() < kSkMaxGrid ? device_sms() : kSkMaxGrid;
@@ -1214,7 +1228,8 @@ SkLayout sk_layout(int B, int Hq) {
   return l;
 }
 
-pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t stream) {
+// One pass: the KV heads p.head_off .. p.head_off + p.Hkv - 1 (of p.Hkv_all).
+static pa_status launch_pass(const DecodeParams& p, void* sk_ws, cudaStream_t stream) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return PA_ERR_UNSUPPORTED;
   const int H = p.Hkv, G = p.Hq / p.Hkv;
@@ -1224,23 +1239,27 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
       p.dtype == PA_BFLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int box_tokens = p.bs < TT ? p.bs : TT;
   CUtensorMap tk, tv, tq;
-  // [blocks][bs][H][D] as a 4-D tensor: a box whose in-block coordinate is
-  // negative reads zeros there instead of the previous block's tokens
+  // [blocks][bs][Hkv_all][D] as a 4-D tensor over this pass's H heads: a box
+  // whose in-block coordinate is negative reads zeros there instead of the
+  // previous block's tokens
   const cuuint64_t kv_dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)p.bs,
                                  (cuuint64_t)p.num_blocks};
-  const cuuint64_t kv_strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2,
-                                    (cuuint64_t)p.bs * H * kD * 2};
+  const cuuint64_t kv_strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)p.Hkv_all * kD * 2,
+                                    (cuuint64_t)p.bs * p.Hkv_all * kD * 2};
   const cuuint32_t kv_box[4] = {64, (cuuint32_t)H, (cuuint32_t)box_tokens, 1};
   const cuuint32_t ones[4] = {1, 1, 1, 1};
-  if (enc(&tk, dt, 4, const_cast<void*>(p.k_pool), kv_dims, kv_strides, kv_box, ones,
+  const size_t head_bytes = (size_t)p.head_off * kD * 2;
+  void* kbase = static_cast<char*>(const_cast<void*>(p.k_pool)) + head_bytes;
+  void* vbase = static_cast<char*>(const_cast<void*>(p.v_pool)) + head_bytes;
+  if (enc(&tk, dt, 4, kbase, kv_dims, kv_strides, kv_box, ones,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return PA_ERR_INVALID_ARG;
-  if (enc(&tv, dt, 4, const_cast<void*>(p.v_pool), kv_dims, kv_strides, kv_box, ones,
+  if (enc(&tv, dt, 4, vbase, kv_dims, kv_strides, kv_box, ones,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return PA_ERR_INVALID_ARG;
-  const cuuint64_t q_dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.B * p.Hq};
+  const cuuint64_t q_dims[2] = {(cuuint64_t)kD, (cuuint64_t)p.B * p.Hq_all};
   const cuuint64_t q_strides[1] = {(cuuint64_t)kD * 2};
   const cuuint32_t q_box[2] = {64, (cuuint32_t)N};
   if (enc(&tq, dt, 2, const_cast<void*>(p.q), q_dims, q_strides, q_box, ones,
@@ -1284,6 +1303,27 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
           ? launch_pdl(combine_sk_kernel<PA_BFLOAT16>, dim3((unsigned)cgrid), 128, 0, stream, sp, grid)
           : launch_pdl(combine_sk_kernel<PA_FLOAT16>, dim3((unsigned)cgrid), 128, 0, stream, sp, grid);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Query heads beyond kMaxHq (G = 16, or wide multi-head attention) run as
+// passes over groups of KV heads; the passes read disjoint heads of every pool
+// row, so the bytes read are the same as one pass over all heads.  Each pass
+// reuses the stream-K area: its main kernel starts after the previous pass's
+// combine has read it (stream order; the main kernel writes nothing before its
+// dependency wait).
+pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t stream) {
+  const int G = p.Hq / p.Hkv;
+  const int hg = heads_per_pass(p.Hkv, G);
+  if (hg == 0) return PA_ERR_UNSUPPORTED;
+  for (int off = 0; off < p.Hkv; off += hg) {
+    DecodeParams pp = p;
+    pp.Hkv = hg;
+    pp.Hq = hg * G;
+    pp.head_off = p.head_off + off;
+    const pa_status st = launch_pass(pp, sk_ws, stream);
+    if (st != PA_OK) return st;
+  }
+  return PA_OK;
 }
 
 }  // namespace pa

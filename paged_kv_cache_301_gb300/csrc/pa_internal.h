@@ -30,6 +30,12 @@ struct DecodeParams {
   // seq_lens[b] - 1 before any load of that token's tile.
   const void* new_k;
   const void* new_v;
+  // Head group served by this launch (the grouped tensor-core kernel splits
+  // wide head counts into passes): KV heads head_off .. head_off + Hkv - 1 of
+  // Hkv_all in every pool and new-token row, query heads head_off * G .. of
+  // Hq_all in every q / out row.  Hkv_all = Hkv, Hq_all = Hq, head_off = 0 for
+  // a launch over all heads.
+  int Hkv_all, Hq_all, head_off;
 };
 
 // The decode kernels; which one serves a call depends on its shape and on the
@@ -52,8 +58,8 @@ bool tc_supported(const DecodeParams& p);
 pa_status launch_decode_tc(const DecodeParams& p, int2* items, int* queue, cudaStream_t stream);
 
 // Tensor-core path, all KV heads of a block per CTA with a stream-K split
-// (head_dim 128, Hkv in {1,2,4,8,16,32}, G in {1,2,4,8}, Hq <= 64, up to
-// 16384 sequences): main + combine.
+// (head_dim 128, G in {1,2,4,8,16}, up to 16384 sequences): main + combine,
+// once per group of KV heads with at most 64 query heads.
 constexpr int kSkMaxGrid = 160;          // persistent CTAs at most (GB300: 152 SMs)
 struct SkLayout {
   size_t prefix_off, wprefix_off, m_off, l_off, acc_off, total;

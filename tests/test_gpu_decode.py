@@ -100,15 +100,22 @@ def test_shapes_with_ragged_tails(pa, dtype, head_dim, bs):
 
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (32, 8), (64, 8), (32, 2), (24, 3),
                                     (16, 1), (8, 1), (2, 2), (16, 2), (32, 32), (64, 32),
-                                    (16, 16), (64, 16), (48, 16)])
+                                    (16, 16), (64, 16), (48, 16), (64, 4), (128, 8), (128, 32),
+                                    (256, 16), (128, 128)])
 def test_query_groupings(pa, hq, hkv):
     """Every grouping the grouped kernel instantiates (1 to 32 KV heads per block:
-    multi-query, grouped and plain multi-head attention) and some it does not."""
+    multi-query, grouped and plain multi-head attention; 16 query heads per KV
+    head; more than 64 query heads, served as passes over groups of KV heads)
+    and one it does not (3 query heads per KV head)."""
     lens = [3, 70, 600, 1300]
     w = _small("llama3_8b", num_seqs=4, num_q_heads=hq, num_kv_heads=hkv, length_kind="fixed",
                lens=tuple(lens), seed=77 + hq + hkv)
     batch = scenarios.fixed_batch(w)
-    got = widen(DeviceBatch(batch).decode(pa))
+    dev = DeviceBatch(batch)
+    if pa.decode_path == "tc":
+        kernel = pa.decode_kernel_for(dev.q, dev.k_pool, dev.tables, int(batch.seq_lens.max()))
+        assert kernel == ("per_head" if hq // hkv == 3 else "grouped"), (hq, hkv, kernel)
+    got = widen(dev.decode(pa))
     assert_close(got, scenarios.decode_f64(batch), f"Hq={hq} Hkv={hkv}")
 
 
