@@ -114,6 +114,16 @@ MHA_7B = Workload(
     name="mha_7b", num_seqs=64, num_q_heads=32, num_kv_heads=32, head_dim=128,
     block_size=16, dtype=BFLOAT16, seed=7, length_kind="uniform", lo=128, hi=4096)
 
+# Llama-3-405B-shaped decode: 128 query heads over 8 KV heads (16 per group).
+LLAMA3_405B = Workload(
+    name="llama3_405b", num_seqs=64, num_q_heads=128, num_kv_heads=8, head_dim=128,
+    block_size=16, dtype=BFLOAT16, seed=8, length_kind="uniform", lo=128, hi=4096)
+
+# Continuous batching with many live requests: 2048 sequences of U[16, 1024] tokens.
+MANY_SEQS = Workload(
+    name="many_seqs", num_seqs=2048, num_q_heads=32, num_kv_heads=8, head_dim=128,
+    block_size=16, dtype=BFLOAT16, seed=9, length_kind="uniform", lo=16, hi=1024)
+
 # Prefill: whole prompts of U[512, 4096] tokens; chunked prefill: the last 512
 # tokens of sequences of U[1024, 8192] tokens whose earlier tokens are cached.
 PREFILL = Workload(
@@ -127,7 +137,7 @@ CHUNKED_PREFILL = Workload(
     prefill="chunk", chunk=512)
 
 WORKLOADS = {w.name: w for w in (TINY, LLAMA3_8B, SHARED_PREFIX, LONG_CONTEXT, RAGGED,
-                                  PREFILL, CHUNKED_PREFILL, MHA_7B)}
+                                  PREFILL, CHUNKED_PREFILL, MHA_7B, LLAMA3_405B, MANY_SEQS)}
 
 
 # ----------------------------------------------------------------------------

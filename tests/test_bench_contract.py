@@ -58,6 +58,9 @@ def test_native_arm_line():
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0 < r["frac"] < 1.5
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    # achieved over the timed region's average call; the isolated call beside it
+    assert abs(r["avg_launch_ms"] - d["ms_per_step"]) < 1e-9
+    assert 0 < r["isolated_call"]["frac"] <= r["frac"] + 0.05
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
