@@ -339,21 +339,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       const bool partial = kc + 63 > pos;        // some of its keys lie past the row
       // the tile's maximum of the visible raw scores (scale > 0 commutes with max);
       // S is read again for the exponentials (registers hold one 32-column chunk)
-      float mt = -CUDART_INF_F;
-      {
-        float sv[64];
-        tmem_ld64(scol, sv);
-        if (!partial) {
+      // S is read from tensor memory once and kept in registers (fewer TMEM
+      // reads competing with the tensor core's); masked keys become -inf
+      float sv[64];
+      tmem_ld64(scol, sv);
+      if (partial) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) mt = fmaxf(mt, sv[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) mt = fmaxf(mt, kc + e <= pos ? sv[e] : -CUDART_INF_F);
-        }
+        for (int e = 0; e < 64; ++e) sv[e] = kc + e <= pos ? sv[e] : -CUDART_INF_F;
       }
-      // the first chunk of the second read overlaps the max exchange
-      uint32_t s0[32];
-      tmem_ld32_start(scol, s0);
+      float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+      for (int e = 0; e < 64; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
+      float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       {   // over the row's two halves
         const int rb = t & 1;
         tl->red_max[k][rb][half][r] = mt;
@@ -375,25 +372,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       float ls = 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
-        float sv[32];
-        if (c0 == 0) {
-          tmem_wait_ld32(s0);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sv[e] = __uint_as_float(s0[e]);
-        } else {
-          tmem_ld32(scol + c0, sv);
-        }
 #pragma unroll
         for (int g = 0; g < 32; g += 16) {
           uint32_t pw[16];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
-            float pa_ = ex2_approx(fmaf(sv[g + e], sl2, neg_m));
-            float pb_ = ex2_approx(fmaf(sv[g + e + 1], sl2, neg_m));
-            if (partial) {
-              pa_ = kc + c0 + g + e <= pos ? pa_ : 0.f;
-              pb_ = kc + c0 + g + e + 1 <= pos ? pb_ : 0.f;
-            }
+            // masked keys hold -inf: p = 0
+            const float pa_ = ex2_approx(fmaf(sv[c0 + g + e], sl2, neg_m));
+            const float pb_ = ex2_approx(fmaf(sv[c0 + g + e + 1], sl2, neg_m));
             ls += pa_ + pb_;
             if (DT == PA_BFLOAT16) {
               // hi = the top 16 bits (truncation), lo = the remainder, truncated
