@@ -29,10 +29,10 @@
 // otherwise p may reach 2^8, which fp32 sums and the hi + lo terms carry as
 // well.  The final division by the row sum removes the choice of max.
 //
-// Roles (576 threads): warp 0 issues TMA (both Q tiles, then K(t), V(t) into a
-// ring of 32 KB stages), warp 1 issues tcgen05.mma, warps 2-9 run tile A's
-// softmax and warps 10-17 tile B's, two warps per row (64 keys and 64 output
-// columns each).  Every wait is bounded.
+// Roles (320 threads): warp 0 issues TMA (both Q tiles, then K(t), V(t) into a
+// ring of 32 KB stages), warp 1 issues tcgen05.mma, warps 2-5 run tile A's
+// softmax and warps 6-9 tile B's, one thread per row (all 128 keys of a tile,
+// all 128 output columns: no exchange between warps).  Every wait is bounded.
 #include <math_constants.h>
 
 #include <mutex>
@@ -53,7 +53,7 @@ constexpr int kSlab = 128 * 128;            // 128 rows x 128 bytes
 constexpr int kTile = 2 * kSlab;            // 128 rows x 256 bytes (D = 128, 16-bit)
 constexpr int kQOff = 0;                    // Q_A, then Q_B
 constexpr int kRingOff = kQOff + 2 * kTile;
-constexpr int kSoftWarps = 16;              // eight per query tile
+constexpr int kSoftWarps = 8;               // four per query tile, one thread per row
 constexpr int kThreads = 64 + 32 * kSoftWarps;
 constexpr float kRescaleLog2 = 8.f;         // raise the running max only past this
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -69,10 +69,7 @@ struct Tail {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full;
   uint64_t s_full[2], p_full[2], pv_done[2];   // per query tile
-  uint64_t red_bar[2][2][4], sum_bar[2][4];    // [tile][parity][lane quarter]
   uint64_t drain;
-  float red_max[2][2][2][128];                 // [tile][parity][half][row]
-  float red_sum[2][2][128];                    // [tile][half][row]
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -138,11 +135,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       mbar_init(&tl->s_full[k], 1);
       mbar_init(&tl->p_full[k], kSoftWarps / 2);
       mbar_init(&tl->pv_done[k], 1);
-      for (int w = 0; w < 4; ++w) {
-        mbar_init(&tl->red_bar[k][0][w], 2);
-        mbar_init(&tl->red_bar[k][1][w], 2);
-        mbar_init(&tl->sum_bar[k][w], 2);
-      }
     }
     mbar_init(&tl->drain, 1);
     tl->abort_flag = 0;
@@ -311,19 +303,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
   else {
     // ------------------------------------------------ softmax and output rows --
-    // Tile k = 0 (A) or 1 (B); two warps per TMEM lane quarter, half 0 with keys
-    // 0-63 of each S tile and output columns 0-63, half 1 with the rest.
-    const int k = (warp - 2) >> 3;
-    const int half = ((warp - 2) >> 2) & 1;
+    // Tile k = 0 (A, warps 2-5) or 1 (B, warps 6-9); warp w reads the TMEM lane
+    // quarter w % 4, so thread r = 32 (w % 4) + lane owns tile row r: all 128 keys
+    // of every S tile (no exchange with another warp) and all 128 output columns.
+    const int k = (warp - 2) >> 2;
     const int wq = warp & 3;                     // TMEM lane quarter of this warp
     const int r = wq * 32 + lane;                // tile row = query token r / G, head r % G
-    const int cb = half * 64;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const int i = (k ? q0b : q0a) + r / G;       // query token within the sequence's queries
     const bool row_valid = i < n;
     const int pos = row_valid ? L - n + i : -1;  // keys 0 .. pos are visible
-    const uint32_t scol = tmem + lane_base + k * kKeys + cb;
-    const uint32_t ocol = tmem + lane_base + 256 + k * kD + cb;
+    const uint32_t scol = tmem + lane_base + k * kKeys;
+    const uint32_t ocol = tmem + lane_base + 256 + k * kD;
     const float sl2 = p.scale_log2;
     float m_run = -CUDART_INF_F, l_run = 0.f;
     bool ok = true;
@@ -335,30 +326,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int t = 0; t <= my_last && ok; ++t) {
       if (!wait_all(&tl->s_full[k], t & 1)) { ok = false; break; }
       tc_fence_after();
-      const int kc = t * kKeys + cb;             // key of this thread's first column
-      const bool partial = kc + 63 > pos;        // some of its keys lie past the row
-      // the tile's maximum of the visible raw scores (scale > 0 commutes with max);
-      // S is read again for the exponentials (registers hold one 32-column chunk)
+      const int kc = t * kKeys;                  // key of column 0
+      const bool partial = kc + kKeys - 1 > pos; // some keys lie past the row
       // S is read from tensor memory once and kept in registers (fewer TMEM
       // reads competing with the tensor core's); masked keys become -inf
-      float sv[64];
-      tmem_ld64(scol, sv);
+      float sv[kKeys];
+      {
+        float h0[64], h1[64];
+        tmem_ld64(scol, h0);
+        tmem_ld64(scol + 64, h1);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          sv[e] = h0[e];
+          sv[64 + e] = h1[e];
+        }
+      }
       if (partial) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) sv[e] = kc + e <= pos ? sv[e] : -CUDART_INF_F;
+        for (int e = 0; e < kKeys; ++e) sv[e] = kc + e <= pos ? sv[e] : -CUDART_INF_F;
       }
       float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-      for (int e = 0; e < 64; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
-      float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      {   // over the row's two halves
-        const int rb = t & 1;
-        tl->red_max[k][rb][half][r] = mt;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->red_bar[k][rb][wq]);
-        if (!wait_all(&tl->red_bar[k][rb][wq], (t >> 1) & 1)) { ok = false; break; }
-        mt = fmaxf(mt, tl->red_max[k][rb][half ^ 1][r]);
-      }
+      for (int e = 0; e < kKeys; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
+      const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float m_tile = mt * sl2;
       // Rows whose max grows by more than 2^8 raise it; O (complete up to tile
       // t-1) and l scale by 2^(m_old - m_new).  TMEM access is warp-wide, so the
@@ -368,46 +358,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (m_run == -CUDART_INF_F || raise) m_run = m_tile;   // first visible tile, or raised
       const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
       // p = 2^(s * scale * log2 e - m), written back over the S columns as
-      // hi / lo storage-type pairs (16-key group: 8 hi words, then 8 lo words)
-      float ls = 0.f;
+      // hi / lo storage-type pairs (16-key group: 8 hi words, then 8 lo words);
+      // masked keys hold -inf and give p = 0
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
+      for (int g = 0; g < kKeys; g += 16) {
+        uint32_t pw[16];
 #pragma unroll
-        for (int g = 0; g < 32; g += 16) {
-          uint32_t pw[16];
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            // masked keys hold -inf: p = 0
-            const float pa_ = ex2_approx(fmaf(sv[c0 + g + e], sl2, neg_m));
-            const float pb_ = ex2_approx(fmaf(sv[c0 + g + e + 1], sl2, neg_m));
-            ls += pa_ + pb_;
-            if (DT == PA_BFLOAT16) {
-              // hi = the top 16 bits (truncation), lo = the remainder, truncated
-              // too: hi + lo carries ~15 significant bits with byte permutes
-              // only (no conversion instruction)
-              const uint32_t ua = __float_as_uint(pa_), ub = __float_as_uint(pb_);
-              pw[e >> 1] = __byte_perm(ua, ub, 0x7632);
-              pw[8 + (e >> 1)] =
-                  __byte_perm(__float_as_uint(pa_ - __uint_as_float(ua & 0xFFFF0000u)),
-                              __float_as_uint(pb_ - __uint_as_float(ub & 0xFFFF0000u)), 0x7632);
-            } else {
-              const uint32_t h2 = narrow2<DT>(pa_, pb_);
-              const float2 hf = widen2<DT>(h2);
-              pw[e >> 1] = h2;
-              pw[8 + (e >> 1)] = narrow2<DT>(pa_ - hf.x, pb_ - hf.y);
-            }
+        for (int e = 0; e < 16; e += 2) {
+          const float pa_ = ex2_approx(fmaf(sv[g + e], sl2, neg_m));
+          const float pb_ = ex2_approx(fmaf(sv[g + e + 1], sl2, neg_m));
+          ls4[(e >> 1) & 3] += pa_ + pb_;
+          if (DT == PA_BFLOAT16) {
+            // hi = the top 16 bits (truncation), lo = the remainder, truncated
+            // too: hi + lo carries ~15 significant bits with byte permutes only
+            // (no conversion instruction)
+            const uint32_t ua = __float_as_uint(pa_), ub = __float_as_uint(pb_);
+            pw[e >> 1] = __byte_perm(ua, ub, 0x7632);
+            pw[8 + (e >> 1)] =
+                __byte_perm(__float_as_uint(pa_ - __uint_as_float(ua & 0xFFFF0000u)),
+                            __float_as_uint(pb_ - __uint_as_float(ub & 0xFFFF0000u)), 0x7632);
+          } else {
+            const uint32_t h2 = narrow2<DT>(pa_, pb_);
+            const float2 hf = widen2<DT>(h2);
+            pw[e >> 1] = h2;
+            pw[8 + (e >> 1)] = narrow2<DT>(pa_ - hf.x, pb_ - hf.y);
           }
-          tmem_st16_nowait(scol + c0 + g, pw);   // over S columns already read
         }
+        tmem_st16_nowait(scol + g, pw);          // over S columns already read
       }
+      const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       // Rows that raised their max rescale O (complete up to tile t-1, P.V(t) not
-      // yet issued) and l.  TMEM access is warp-wide: the warp rescales when any
-      // of its rows needs it (the others by 1).
+      // yet issued) and l.
       if (__any_sync(0xFFFFFFFFu, raise)) {
         if (!wait_all(&tl->pv_done[k], (t - 1) & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
+        for (int c0 = 0; c0 < kD; c0 += 32) {
           float o[32];
           tmem_ld32(ocol + c0, o);
           uint32_t ow[32];
@@ -420,15 +407,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       // keys at or past L: their V rows hold whatever the slot or an earlier tile
       // left (0 * NaN must not reach O).  The first tile whose product reads V(t)
       // zeroes them before releasing its P.
-      const int k0 = t * kKeys;
-      if (k0 + kKeys > L && (k == 0 || t > last_a)) {
+      if (kc + kKeys > L && (k == 0 || t > last_a)) {
         const int u = 2 * t + 1;
         if (!wait_all(&tl->full[u % kStages], (u / kStages) & 1)) { ok = false; break; }
-        if (k0 + r >= L) {                       // V row r: this warp zeroes one 64-column slab
-          uint4* v0 = reinterpret_cast<uint4*>(smem + kRingOff + (u % kStages) * kTile +
-                                               half * kSlab + r * 128);
+        if (kc + r >= L) {                       // V row r, both 64-column slabs
+          uint4* v0 = reinterpret_cast<uint4*>(smem + kRingOff + (u % kStages) * kTile + r * 128);
+          uint4* v1 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(v0) + kSlab);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v0[e] = make_uint4(0, 0, 0, 0);
+          for (int e = 0; e < 8; ++e) {
+            v0[e] = make_uint4(0, 0, 0, 0);
+            v1[e] = make_uint4(0, 0, 0, 0);
+          }
         }
       }
       // consume P.V(t-1)'s completion before P(t) is released, so the barrier
@@ -442,22 +431,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     if (my_last >= 0) {
       if (ok) ok = wait_all(&tl->pv_done[k], my_last & 1);
-      if (ok) {   // row sum over both halves
-        tl->red_sum[k][half][r] = l_run;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->sum_bar[k][wq]);
-        ok = wait_all(&tl->sum_bar[k][wq], 0);
-      }
       if (!ok) {
         if (lane == 0) set_abort();
       } else {
         tc_fence_after();
-        const float inv = 1.f / (l_run + tl->red_sum[k][half ^ 1][r]);
+        const float inv = 1.f / l_run;
         uint4* dst = reinterpret_cast<uint4*>(
             static_cast<uint16_t*>(p.out) + ((int64_t)(qs + (row_valid ? i : 0)) * p.Hq + h * G +
-                                             r % G) * kD + cb);
+                                             r % G) * kD);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
+        for (int c0 = 0; c0 < kD; c0 += 32) {
           float o[32];
           tmem_ld32(ocol + c0, o);
           if (row_valid) {

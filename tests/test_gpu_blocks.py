@@ -164,3 +164,22 @@ def test_swap_bad_ids_reported_and_skipped(pa):
     assert int(status.item()) == 5
     for c, b in zip(cpu, cbits):
         assert np.array_equal(_cpu_bits(c), b)
+
+
+def test_stream_read_reads_every_byte():
+    """pa_stream_read (the benchmark's read-stream context) counts, per thread,
+    the words whose XOR equals 0x9E3779B9: in a zero buffer holding that word at
+    the start, the middle and the end (and in the tail that does not fill a whole
+    round of the grid), the sink counts three, so every region was read."""
+    import torch
+    from tests.gpu_helpers import lib
+    pa = lib()
+    n_words = (3 << 20) + 20                 # 12 MiB + 80 bytes: a ragged tail
+    buf = torch.zeros(n_words, dtype=torch.int32, device="cuda")
+    magic = 0x9E3779B9 - (1 << 32)           # as int32
+    for i in (0, n_words // 2 + 4, n_words - 1):
+        buf[i] = magic
+    sink = torch.zeros(1, dtype=torch.int64, device="cuda")
+    pa.pa_stream_read(buf, sink)
+    torch.cuda.synchronize()
+    assert int(sink.item()) == 3
