@@ -416,9 +416,11 @@ def workload_config(w, lens, num_blocks, args) -> dict:
         "total_tokens": int(np.sum(lens)), "num_blocks": int(num_blocks),
         "partition_tokens": args.partition_tokens or 512,
         "kv_bytes_per_step": kvb,
-        "l2": f"inputs larger than L2: {kvb / 2**20:.0f} MiB of K/V read per step vs "
-              f"{L2_BYTES / 2**20:.0f} MiB L2; no flush between steps (the l2_flushed "
-              f"figure flushes before each call)",
+        "l2": (f"inputs larger than L2: {kvb / 2**20:.0f} MiB of K/V read per step vs "
+               f"{L2_BYTES / 2**20:.0f} MiB L2; no flush between steps (the l2_flushed "
+               f"figure flushes before each call)") if kvb > L2_BYTES else
+              (f"{kvb / 2**10:.0f} KiB of K/V per step, resident in L2: a latency-bound "
+               f"step (no roofline target), no flush"),
         "parallelism": f"replicas x{args.world}" if args.world > 1 else "1 GPU",
     }
 
@@ -766,7 +768,7 @@ def measure_stream_read(torch, pa, dev, args) -> dict:
 
 
 # Workloads measured beside the headline one in a default run.
-EXTRA_WORKLOADS = ("long_context", "shared_prefix", "ragged")
+EXTRA_WORKLOADS = ("long_context", "shared_prefix", "ragged", "tiny")
 
 
 def run_native(args, dist_info):

@@ -47,7 +47,8 @@ def test_native_arm_line():
     assert d["gpu_launches_per_step"] == 2 and d["repeats"] >= 25
     assert d["gpu_launches"] == 2 * 20 * d["repeats"]
     # every other decode workload, prefill and the read stream in the same line
-    assert {"long_context", "shared_prefix", "ragged", "prefill"} <= set(d["workloads"])
+    assert {"long_context", "shared_prefix", "ragged", "tiny", "prefill"} <= set(d["workloads"])
+    assert d["workloads"]["tiny"]["ms_per_step"] > 0         # latency-bound: no roofline target
     for name in ("long_context", "shared_prefix", "ragged"):
         x = d["workloads"][name]
         assert x["config"]["workload"] == name and x["value"] > 0 and x["tokens_per_s"] > 0
