@@ -142,8 +142,9 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
  * Three decode kernels exist:
  *   grouped tensor-core kernel (tcgen05 + TMA): each CTA reads whole blocks,
  *     all KV heads at once, over an equal share of the batch's tokens;
- *     head_dim 128, num_kv_heads in {1,2,4,8,16,32}, num_q_heads / num_kv_heads
- *     in {1,2,4,8}, num_q_heads <= 64, num_seqs <= 16384;
+ *     head_dim 128, num_q_heads / num_kv_heads in {1,2,4,8,16}, num_seqs <=
+ *     16384; more than 64 query heads run as passes over groups of 1-32 KV
+ *     heads (a group must divide num_kv_heads);
  *   per-head tensor-core kernel (tcgen05 + TMA): one KV head per work item;
  *     head_dim 128, any grouping;
  *   CUDA-core kernel: every supported shape.
