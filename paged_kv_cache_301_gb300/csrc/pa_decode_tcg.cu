@@ -18,16 +18,19 @@
 // P' is stored as two storage-type terms (hi + lo, ~16 significant bits).
 //
 // Work split (stream-K): the batch is a sequence of token tiles, each sequence
-// padded to whole tiles.  A sequence weighs kStartWeight + its tiles (starting
-// a sequence costs a CTA about one tile's time: its epilogue and the next
-// sequence's first copies), and CTA c of the persistent grid takes the tiles
-// whose weighted positions fall in [c*W/grid, (c+1)*W/grid), W the batch's
-// total weight.  A sequence that lies inside one CTA's range is written
-// directly; a sequence cut by range boundaries leaves one partial (max, sum,
-// accumulator) per CTA, merged by the combine kernel.  Every CTA gets the same
-// weight to within one, whatever the length mix.  Each CTA keeps in shared
-// memory only the window of sequences its range meets, so the batch size is
-// not bounded by shared memory.
+// padded to whole tiles.  A sequence weighs a start weight sw + its tiles
+// (starting a sequence costs a CTA about one tile's time: its epilogue and the
+// next sequence's first copies, so sw = 1), and CTA c of the persistent grid
+// takes the tiles whose weighted positions fall in [c*W/grid, (c+1)*W/grid), W
+// the batch's total weight.  Every CTA gets the same weight to within one,
+// whatever the length mix.  A sequence that lies inside one CTA's range is
+// written directly; a sequence cut by range boundaries leaves one partial
+// (max, sum, accumulator) per CTA, merged by the combine kernel.  Each CTA
+// keeps in shared memory only the window of sequences its range meets (at most
+// kWin), so the batch size is not bounded by shared memory.  A range of R units
+// meets at most R / (sw + 1) + 2 sequences; in a batch so long that R / 2 + 2
+// could exceed kWin (more than ~190K tiles, i.e. > 6 GB of K/V, beside hundreds
+// of short sequences), sw is raised until it cannot.
 //
 // Roles (192 threads, one CTA per SM): warp 0 issues TMA, warp 1 issues MMA,
 // warps 2-5 run the softmax and the epilogue (and, in pa_decode_append, the
@@ -131,7 +134,7 @@ constexpr int smem_bytes() {
 struct SkParams {
   DecodeParams p;
   int* tile_prefix;         // [B + 1] tiles before sequence b (written by CTA 0 for the combine)
-  int* weight_prefix;       // [B + 1] weight before sequence b (written by CTA 0 for the combine)
+  int* weight_prefix;       // [B + 2] weight before sequence b, then the start weight (the same)
   float* part_m;            // [grid * 2 * Hq]
   float* part_l;
   float* part_acc;          // [grid * 2 * Hq * D]
@@ -283,14 +286,23 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       T += tl->scan[0][w];
       NE += tl->scan[1][w];
     }
-    const int W = T + kStartWeight * NE;
+    // start weight: the least >= kStartWeight with (T + sw NE) / grid + 1 <=
+    // (kWin - 2)(sw + 1), so that no range meets more than kWin sequences (the
+    // host keeps NE <= (kWin - 2) grid / 2, so den > 0)
+    int sw = kStartWeight;
+    {
+      const long long num = (long long)T + grid - (long long)(kWin - 2) * grid;
+      const long long den = (long long)(kWin - 2) * grid - NE;
+      if (num > 0) sw = max(sw, (int)((num + den - 1) / den));
+    }
+    const int W = T + sw * NE;
     const int x0 = range_start(c, W, grid), x1 = range_start(c + 1, W, grid);
     const int first_t = run_t, first_n = run_n;
     for (int b = b0; b < b1; ++b) {
       const int raw = p.seq_lens[b];
       const int L = clamp_len(p, b);
       const int nt = (L + TT - 1) / TT;
-      const int run_w = run_t + kStartWeight * run_n;
+      const int run_w = run_t + sw * run_n;
       if (c == 0) {
         sp.tile_prefix[b] = run_t;
         sp.weight_prefix[b] = run_w;
@@ -302,11 +314,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (p.new_k != nullptr) store_newest<H>(p, b, 0, 1);   // no tile reads it
       }
       if (nt > 0) {
-        // weighted span [run_w, run_w + kStartWeight + nt): the start, then the
+        // weighted span [run_w, run_w + sw + nt): the start, then the
         // tiles; a cut in it falls before tile clamp(x - run_w - start, 0, nt)
-        const int span_end = run_w + kStartWeight + nt;
+        const int span_end = run_w + sw + nt;
         if (run_w <= x0 && x0 < span_end) {
-          const int tb = run_t + min(max(x0 - run_w - kStartWeight, 0), nt);
+          const int tb = run_t + min(max(x0 - run_w - sw, 0), nt);
           tl->cut[0] = tb;
           // the window starts at the sequence holding tile tb (tb < run_t + nt
           // here); its first block ids go to L2 now, so that the producer's
@@ -318,7 +330,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
           if (kf + 32 < p.max_blocks) prefetch_l2(ids + 32);
         }
         if (run_w <= x1 && x1 < span_end) {
-          const int te = run_t + min(max(x1 - run_w - kStartWeight, 0), nt);
+          const int te = run_t + min(max(x1 - run_w - sw, 0), nt);
           tl->cut[1] = te;
           tl->win_n[1] = te > run_t ? run_n + 1 : run_n;   // sequences before the end cut
         }
@@ -329,7 +341,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     if (et == 127) {
       if (c == 0) {
         sp.tile_prefix[p.B] = run_t;
-        sp.weight_prefix[p.B] = run_t + kStartWeight * run_n;
+        sp.weight_prefix[p.B] = run_t + sw * run_n;
+        sp.weight_prefix[p.B + 1] = sw;
       }
       if (x0 >= W) {              // cuts at the batch's end (or an empty batch)
         tl->cut[0] = T;
@@ -1009,13 +1022,13 @@ combine_sk_kernel(const SkParams sp, int grid) {
   const int64_t row = (int64_t)blockIdx.x * 4 + warp;
   if (row >= (int64_t)p.B * p.Hq) return;
   const int b = (int)(row / p.Hq), q = (int)(row - (int64_t)b * p.Hq);
-  const int W = sp.weight_prefix[p.B];
+  const int W = sp.weight_prefix[p.B], sw = sp.weight_prefix[p.B + 1];
   const int tpb = sp.tile_prefix[b], tpb1 = sp.tile_prefix[b + 1];
   const int pwb = sp.weight_prefix[b];
   if (tpb1 <= tpb) return;                                  // empty: zeroed by the main kernel
-  // weighted position of the sequence's tile j: pwb + kStartWeight + j
-  const int cf = range_owner(pwb + kStartWeight, W, grid);
-  const int cl = range_owner(pwb + kStartWeight + (tpb1 - tpb) - 1, W, grid);
+  // weighted position of the sequence's tile j: pwb + sw + j
+  const int cf = range_owner(pwb + sw, W, grid);
+  const int cl = range_owner(pwb + sw + (tpb1 - tpb) - 1, W, grid);
   if (cf == cl) return;                                     // written directly
   const int nparts = cl - cf + 1;
   // part i: CTA cf + i, slot 0 when the sequence is that CTA's first segment
@@ -1206,12 +1219,13 @@ bool tcg_supported(const DecodeParams& p) {
   // a bad block id is redirected to row num_blocks * bs (+ offset < 64): stays an int
   if ((long long)p.num_blocks * p.bs + 64 >= (1ll << 31)) return false;
   if ((long long)p.B * p.Hq >= (1ll << 31)) return false;
-  // the batch's weight (tiles + one per sequence) stays an int
-  const long long TT = kRows / hg;
-  if ((long long)p.B * ((p.max_seq_len + TT - 1) / TT + kStartWeight) >= (1ll << 31)) return false;
-  // a CTA's range meets at most B / grid + 2 sequences: they fit its window
+  // The start weight keeps every range within its window when B <= (kWin - 2)
+  // grid / 2; it is then at most T / den + 1 with den >= B, so the batch's
+  // weight T + sw B <= 2 T + B stays an int.
   const int grid = device_sms() < kSkMaxGrid ? device_sms() : kSkMaxGrid;
-  if (grid <= 0 || (long long)p.B > (long long)(kWin - 2) * grid) return false;
+  if (grid <= 0 || 2ll * p.B > (long long)(kWin - 2) * grid) return false;
+  const long long TT = kRows / hg;
+  if (2ll * p.B * ((p.max_seq_len + TT - 1) / TT + 1) >= (1ll << 31)) return false;
   return encode_fn() != nullptr;
 }
 
@@ -1220,7 +1234,7 @@ SkLayout sk_layout(int B, int Hq) {
   SkLayout l;
   l.prefix_off = 0;
   l.wprefix_off = l.prefix_off + a((size_t)(B + 1) * sizeof(int));
-  l.m_off = l.wprefix_off + a((size_t)(B + 1) * sizeof(int));
+  l.m_off = l.wprefix_off + a((size_t)(B + 2) * sizeof(int));
   const size_t parts = (size_t)kSkMaxGrid * 2 * Hq;
   l.l_off = l.m_off + a(parts * sizeof(float));
   l.acc_off = l.l_off + a(parts * sizeof(float));

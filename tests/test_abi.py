@@ -107,11 +107,11 @@ def test_workspace_size(lib):
     rows = 64 * 32 * P
     a = lambda x: (x + 255) // 256 * 256
     # per-head path: queue counters, (sequence, partition) list, m, l, acc;
-    # grouped path: tile and weight prefixes and the partials of up to 160 CTAs
-    # x 2 segments x Hq heads
+    # grouped path: tile prefixes, weight prefixes and the start weight, and the
+    # partials of up to 160 CTAs x 2 segments x Hq heads
     per_head = 256 + a(64 * P * 8) + 2 * a(rows * 4) + a(rows * 128 * 4)
     parts = 160 * 2 * 32
-    grouped = 2 * a(65 * 4) + 2 * a(parts * 4) + a(parts * 128 * 4)
+    grouped = a(65 * 4) + a(66 * 4) + 2 * a(parts * 4) + a(parts * 128 * 4)
     # enough for whichever kernel runs (each lays out its own parts from 0)
     assert n == max(per_head, grouped)
     assert lib.pa_decode_workspace_bytes(64, 32, 128, 4096, 100) == 0

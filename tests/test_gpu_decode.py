@@ -313,9 +313,9 @@ def test_more_kv_heads_per_block_ragged(pa, hq, hkv, bs):
 
 def test_workspace_of_exactly_the_grouped_kernels_size(pa):
     """The grouped kernel's workspace is its stream-K area only (tile and weight
-    prefixes, per-CTA (max, sum) and accumulators of up to 160 CTAs x 2 segments), whatever
-    the lengths: pa_decode runs with exactly that many bytes and refuses one
-    fewer; the result matches the oracle."""
+    prefixes, the start weight, per-CTA (max, sum) and accumulators of up to 160
+    CTAs x 2 segments), whatever the lengths: pa_decode runs with exactly that
+    many bytes and refuses one fewer; the result matches the oracle."""
     if pa.decode_path != "tc":
         pytest.skip("the grouped kernel's layout")
     w = syn.LLAMA3_8B.__class__(**{**syn.LLAMA3_8B.__dict__, "num_seqs": 12, "hi": 1500,
@@ -327,8 +327,8 @@ def test_workspace_of_exactly_the_grouped_kernels_size(pa):
     n = pa.pa_decode_workspace_bytes_for(B, Hq, w.num_kv_heads, D, w.block_size,
                                          dev.tables.shape[1], batch.num_blocks, max_len, 1)
     parts = 160 * 2 * Hq
-    assert n == 2 * (-(-4 * (B + 1) // 256) * 256) + 2 * (-(-4 * parts // 256) * 256) + \
-        (-(-4 * parts * D // 256) * 256)
+    assert n == (-(-4 * (B + 1) // 256) * 256) + (-(-4 * (B + 2) // 256) * 256) + \
+        2 * (-(-4 * parts // 256) * 256) + (-(-4 * parts * D // 256) * 256)
     ws = torch.empty(n, dtype=torch.uint8, device="cuda")
     out = torch.empty_like(dev.q)
     pa.pa_decode(out, dev.q, dev.k_pool, dev.v_pool, dev.tables, dev.lens, batch.scale,
@@ -357,3 +357,102 @@ def test_ten_thousand_tiny_sequences(pa):
     assert np.isfinite(got).all()
     rows = sorted(set(list(range(0, B, 97)) + list(range(4990, 5030)) + [B - 1]))
     assert_close(got[rows], scenarios.decode_f64(batch, sequences=rows)[rows], "B=10000")
+
+
+@pytest.mark.parametrize("hq,hkv,lens", [
+    (32, 8, (60000,)),                    # one sequence over every CTA
+    (32, 8, (20000, 100, 9000)),          # two sequences over dozens of CTAs each
+    (128, 8, (30000, 7)),                 # 16 query heads per KV head: two passes
+    (64, 8, (3000,) * 40),                # parts of up to 5 CTAs, most CTAs cut two
+])
+def test_sequences_cut_into_many_parts(pa, hq, hkv, lens):
+    """Sequences cut into many parts by the grouped kernel's split (a CTA's
+    share is ~W / 152 tiles), merged by the combine kernel: every row against
+    the oracle, and a second call with the same workspace gives identical bits."""
+    w = _small("llama3_8b", num_seqs=len(lens), num_q_heads=hq, num_kv_heads=hkv,
+               length_kind="fixed", lens=tuple(lens), seed=900 + hq + len(lens))
+    batch = scenarios.fixed_batch(w)
+    dev = DeviceBatch(batch)
+    max_len = int(batch.seq_lens.max())
+    ws = pa.workspace_for(dev.q, dev.k_pool, dev.tables, max_len)
+    outs = []
+    for _ in range(2):
+        out = torch.empty_like(dev.q)
+        pa.pa_decode(out, dev.q, dev.k_pool, dev.v_pool, dev.tables, dev.lens, batch.scale,
+                     max_seq_len=max_len, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert_close(widen(outs[0]), scenarios.decode_f64(batch), f"Hq={hq} lens={lens[:3]}")
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_one_workspace_serves_every_kernel_in_turn():
+    """One workspace passed to every decode kernel in turn, over batches with
+    different cuts: nothing a call leaves in it affects the next call, whichever
+    kernel either runs."""
+    pa = lib()
+    w1 = dataclasses.replace(syn.LLAMA3_8B, num_seqs=24, lo=100, hi=4000, seed=61)
+    w2 = dataclasses.replace(syn.LLAMA3_8B, num_seqs=7, lo=2000, hi=9000, seed=62)
+    batches = [scenarios.fixed_batch(w) for w in (w1, w2)]
+    ws = pa.alloc_workspace(24, 32, 128, 9000)
+    try:
+        for path in ("tc", "simt", "tc", "tc_head", "tc", "tc"):
+            pa.set_decode_path(path)
+            for batch in batches:
+                dev = DeviceBatch(batch)
+                out = torch.empty_like(dev.q)
+                pa.pa_decode(out, dev.q, dev.k_pool, dev.v_pool, dev.tables, dev.lens,
+                             batch.scale, max_seq_len=int(batch.seq_lens.max()), workspace=ws)
+                torch.cuda.synchronize()
+                assert_close(widen(out), scenarios.decode_f64(batch),
+                             f"{path}, batch of {len(batch.seq_lens)}")
+    finally:
+        pa.set_decode_path("auto")
+
+
+def test_short_sequences_beside_one_very_long_sequence():
+    """700 one-token sequences ahead of one 3.2M-token sequence (32/8 heads, bs
+    16): with one unit of weight per sequence start, the first CTA's equal share
+    of the grouped kernel's split would meet ~660 sequences, more than the 640
+    its window holds; the kernel raises the start weight for such batches.
+    Closed forms check the result: a one-token sequence's output is its V row,
+    bit for bit; with every key zero the long sequence's weights are uniform, so
+    its output is the mean of its V rows (fp64, on the CPU)."""
+    pa = lib()
+    n_short, L, Hq, Hkv, D, bs = 700, 3_200_000, 32, 8, 128, 16
+    nb_long = L // bs
+    NB = nb_long + n_short + 1
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = nb_long + n_short                 # 16 tokens per 128-row tile
+    assert (-(-(tiles + n_short + 1) // min(grid, 160))) // 2 > 640
+    rng = np.random.default_rng(4711)
+    tables = np.full((n_short + 1, nb_long), NB - 1, np.int32)
+    tables[:n_short, 0] = nb_long + rng.permutation(n_short)
+    tables[n_short] = rng.permutation(nb_long)
+    lens = np.array([1] * n_short + [L], np.int32)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4711)
+    k_pool = torch.zeros((NB, bs, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    v_pool = torch.empty((NB, bs, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    for i in range(0, NB, 20000):
+        n = min(20000, NB - i)
+        v_pool[i:i + n] = torch.randn((n, bs, Hkv, D), generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn((n_short + 1, Hq, D), generator=g, device="cuda").to(torch.bfloat16)
+    t_dev, l_dev = i32(tables), i32(lens)
+    pa.set_decode_path("tc")
+    try:
+        assert pa.decode_kernel_for(q, k_pool, t_dev, L) == "grouped"
+        out = torch.empty_like(q)
+        pa.pa_decode(out, q, k_pool, v_pool, t_dev, l_dev, D ** -0.5, max_seq_len=L)
+        torch.cuda.synchronize()
+    finally:
+        pa.set_decode_path("auto")
+    got = to_host_bits(out)
+    rows = to_host_bits(v_pool[nb_long:nb_long + n_short, 0])        # [n_short, Hkv, D]
+    want = rows[tables[:n_short, 0] - nb_long].repeat(Hq // Hkv, axis=1)
+    assert np.array_equal(got[:n_short], want)
+    total = torch.zeros((Hkv, D), dtype=torch.float64)
+    for i in range(0, nb_long, 20000):
+        total += v_pool[i:min(nb_long, i + 20000)].cpu().double().sum(dim=(0, 1))
+    mean = (total / L).numpy().repeat(Hq // Hkv, axis=0)
+    assert_close(widen(out)[n_short], mean, "long sequence: mean of its V rows")
