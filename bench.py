@@ -768,7 +768,12 @@ def measure_stream_read(torch, pa, dev, args) -> dict:
 
 
 # Workloads measured beside the headline one in a default run.
-EXTRA_WORKLOADS = ("long_context", "shared_prefix", "ragged", "tiny")
+# The other workloads of the default line: (entry, workload, block size or None
+# for the workload's own); the ragged step at every block size it sweeps.
+EXTRA_WORKLOADS = (("long_context", "long_context", None), ("shared_prefix", "shared_prefix", None),
+                   ("ragged", "ragged", None), ("ragged_bs8", "ragged", 8),
+                   ("ragged_bs32", "ragged", 32), ("ragged_bs64", "ragged", 64),
+                   ("tiny", "tiny", None))
 
 
 def run_native(args, dist_info):
@@ -797,8 +802,8 @@ def run_native(args, dist_info):
     workloads = {}
     stream_read = None
     if args.workload == "llama3_8b" and not args.single_workload:
-        for name in EXTRA_WORKLOADS:
-            wx = workload(name, None)
+        for name, wname, wbs in EXTRA_WORKLOADS:
+            wx = workload(wname, wbs)
             st = NativeStep(pa, torch, wx, dev, args.partition_tokens, args.kernel,
                             fused=not args.split_step)
             workloads[name] = decode_entry(st, measure_decode(torch, st, args, world, dev,

@@ -47,9 +47,10 @@ def test_native_arm_line():
     assert d["gpu_launches_per_step"] == 2 and d["repeats"] >= 25
     assert d["gpu_launches"] == 2 * 20 * d["repeats"]
     # every other decode workload, prefill and the read stream in the same line
-    assert {"long_context", "shared_prefix", "ragged", "tiny", "prefill"} <= set(d["workloads"])
+    assert {"long_context", "shared_prefix", "ragged", "ragged_bs8", "ragged_bs32", "ragged_bs64",
+            "tiny", "prefill"} <= set(d["workloads"])
     assert d["workloads"]["tiny"]["ms_per_step"] > 0         # latency-bound: no roofline target
-    for name in ("long_context", "shared_prefix", "ragged"):
+    for name in ("long_context", "shared_prefix", "ragged", "ragged_bs8", "ragged_bs32", "ragged_bs64"):
         x = d["workloads"][name]
         assert x["config"]["workload"] == name and x["value"] > 0 and x["tokens_per_s"] > 0
         assert x["roofline"]["bound"] == "hbm" and 0 < x["roofline"]["frac"] < 1.5
