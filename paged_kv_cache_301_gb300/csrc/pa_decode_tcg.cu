@@ -58,9 +58,9 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 232448 - 1024;   // per-block limit minus alignment slack
-constexpr int kStartWeight = 1;              // a sequence start weighs one tile in the split
+constexpr int kStartWeight = 1;              // least start weight: a sequence start ~ one tile
 constexpr int kWin = 640;                    // sequences of one CTA's range (shared memory)
-constexpr int kMaxSeqs = 16384;              // batch size served: B / grid + 2 <= kWin
+constexpr int kMaxSeqs = 16384;              // batch size served (also B <= (kWin - 2) grid / 2)
 
 
 struct SegInfo {
