@@ -345,9 +345,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
         for (int e = 0; e < kKeys; ++e) sv[e] = kc + e <= pos ? sv[e] : -CUDART_INF_F;
       }
+      // the softmax is bound by instruction issue: three-input max, and packed
+      // two-wide fp32 arithmetic below
       float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-      for (int e = 0; e < kKeys; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
+      for (int e = 0; e < kKeys; e += 8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mx4[c] = fmax3(mx4[c], sv[e + 2 * c], sv[e + 2 * c + 1]);
+      }
       const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float m_tile = mt * sl2;
       // Rows whose max grows by more than 2^8 raise it; O (complete up to tile
@@ -360,24 +365,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
       // p = 2^(s * scale * log2 e - m), written back over the S columns as
       // hi / lo storage-type pairs (16-key group: 8 hi words, then 8 lo words);
       // masked keys hold -inf and give p = 0
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
+      uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int g = 0; g < kKeys; g += 16) {
         uint32_t pw[16];
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
-          const float pa_ = ex2_approx(fmaf(sv[g + e], sl2, neg_m));
-          const float pb_ = ex2_approx(fmaf(sv[g + e + 1], sl2, neg_m));
-          ls4[(e >> 1) & 3] += pa_ + pb_;
+          float ta, tb;
+          f2_unpack(f2_fma(f2_pack(sv[g + e], sv[g + e + 1]), sl2x2, negm2), ta, tb);
+          const float pa_ = ex2_approx(ta);
+          const float pb_ = ex2_approx(tb);
+          const uint64_t p2 = f2_pack(pa_, pb_);
+          ls2[(e >> 1) & 1] = f2_add(ls2[(e >> 1) & 1], p2);
           if (DT == PA_BFLOAT16) {
             // hi = the top 16 bits (truncation), lo = the remainder, truncated
             // too: hi + lo carries ~15 significant bits with byte permutes only
             // (no conversion instruction)
             const uint32_t ua = __float_as_uint(pa_), ub = __float_as_uint(pb_);
             pw[e >> 1] = __byte_perm(ua, ub, 0x7632);
-            pw[8 + (e >> 1)] =
-                __byte_perm(__float_as_uint(pa_ - __uint_as_float(ua & 0xFFFF0000u)),
-                            __float_as_uint(pb_ - __uint_as_float(ub & 0xFFFF0000u)), 0x7632);
+            float ra, rb;
+            f2_unpack(f2_sub(p2, f2_pack(__uint_as_float(ua & 0xFFFF0000u),
+                                         __uint_as_float(ub & 0xFFFF0000u))), ra, rb);
+            pw[8 + (e >> 1)] = __byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x7632);
           } else {
             const uint32_t h2 = narrow2<DT>(pa_, pb_);
             const float2 hf = widen2<DT>(h2);
@@ -387,6 +397,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         tmem_st16_nowait(scol + g, pw);          // over S columns already read
       }
+      float ls4[4];
+      f2_unpack(ls2[0], ls4[0], ls4[1]);
+      f2_unpack(ls2[1], ls4[2], ls4[3]);
       const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       // Rows that raised their max rescale O (complete up to tile t-1, P.V(t) not
       // yet issued) and l.
