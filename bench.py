@@ -1287,7 +1287,8 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="llama3_8b",
                     choices=["llama3_8b", "long_context", "shared_prefix", "ragged", "tiny",
-                             "mha_7b", "llama3_405b", "many_seqs", "prefill", "chunked_prefill"])
+                             "mha_7b", "llama3_405b", "many_seqs", "qwen25_32b", "prefill",
+                             "chunked_prefill"])
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_head"], default="auto")

@@ -119,7 +119,8 @@ struct Geo {
   static constexpr int kFree =
       kSmemBudget - (int)sizeof(Tail<N>) - kQBufs * kQBytes - kPBufs * kPBytes;
   static constexpr int kStages = kFree / kStage > kMaxStages ? kMaxStages : kFree / kStage;
-  static constexpr uint32_t kTmemCols = 4 * N < 64 ? 64 : 4 * N;
+  // S and O^T, two slots each: 4N columns, allocated as a power of two
+  static constexpr uint32_t kTmemCols = 4 * N <= 64 ? 64 : 4 * N <= 128 ? 128 : 4 * N <= 256 ? 256 : 512;
   static constexpr int kRingOff = 0;
   static constexpr int kQOff = kStages * kStage;
   static constexpr int kPOff = kQOff + kQBufs * kQBytes;
@@ -1173,6 +1174,11 @@ pa_status launch_hg(const SkParams& sp, const CUtensorMap& k, const CUtensorMap&
   else return PA_ERR_UNSUPPORTED;
 }
 
+// Query heads per KV head other than a power of two (3, 5, 6, 7: e.g. 40 / 8 or
+// 28 / 4 heads) are built for 4 and 8 KV heads per pass only.
+template <int H>
+constexpr bool odd_groups_built() { return H == 4 || H == 8; }
+
 template <int DT, int H>
 pa_status launch_h(int G, const SkParams& sp, const CUtensorMap& k, const CUtensorMap& v,
                    const CUtensorMap& q, int grid, cudaStream_t stream) {
@@ -1182,8 +1188,18 @@ pa_status launch_h(int G, const SkParams& sp, const CUtensorMap& k, const CUtens
     case 4: return launch_hg<DT, H, 4>(sp, k, v, q, grid, stream);
     case 8: return launch_hg<DT, H, 8>(sp, k, v, q, grid, stream);
     case 16: return launch_hg<DT, H, 16>(sp, k, v, q, grid, stream);
-    default: return PA_ERR_UNSUPPORTED;
+    default: break;
   }
+  if constexpr (odd_groups_built<H>()) {
+    switch (G) {
+      case 3: return launch_hg<DT, H, 3>(sp, k, v, q, grid, stream);
+      case 5: return launch_hg<DT, H, 5>(sp, k, v, q, grid, stream);
+      case 6: return launch_hg<DT, H, 6>(sp, k, v, q, grid, stream);
+      case 7: return launch_hg<DT, H, 7>(sp, k, v, q, grid, stream);
+      default: break;
+    }
+  }
+  return PA_ERR_UNSUPPORTED;
 }
 
 // KV heads per block: a tile is 128 rows = 128 / H tokens x H heads
@@ -1203,20 +1219,25 @@ pa_status launch_dt(int H, int G, const SkParams& sp, const CUtensorMap& k, cons
 
 }  // namespace
 
+static bool pow2_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
+
 // KV heads per pass: all of them when their query heads fit one pass (thread d
 // of the softmax warps keeps one accumulator per query head, at most kMaxHq),
 // else the largest group of 1, 2, 4, 8, 16 or 32 heads that divides Hkv and
-// whose query heads fit; 0 when none does.
+// whose query heads fit (for G of 3, 5, 6 or 7: a group of 8 or 4 heads, the
+// ones built); 0 when none does.
 int heads_per_pass(int Hkv, int G) {
+  const bool odd = !pow2_group(G);
+  if (odd && G != 3 && G != 5 && G != 6 && G != 7) return 0;
   for (int hg = 32; hg >= 1; hg >>= 1)
-    if (hg <= Hkv && Hkv % hg == 0 && hg * G <= kMaxHq) return hg;
+    if (hg <= Hkv && Hkv % hg == 0 && hg * G <= kMaxHq && (!odd || hg == 4 || hg == 8))
+      return hg;
   return 0;
 }
 
 bool tcg_supported(const DecodeParams& p) {
   const int G = p.Hq / p.Hkv;
   if (p.D != kD) return false;
-  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return false;
   const int hg = heads_per_pass(p.Hkv, G);
   if (hg == 0) return false;
   if (p.B > kMaxSeqs) return false;

@@ -119,6 +119,12 @@ LLAMA3_405B = Workload(
     name="llama3_405b", num_seqs=64, num_q_heads=128, num_kv_heads=8, head_dim=128,
     block_size=16, dtype=BFLOAT16, seed=8, length_kind="uniform", lo=128, hi=4096)
 
+# Five query heads per KV head (Qwen2.5-32B's 40 query / 8 KV heads), the
+# Llama-3-8B-shaped lengths.
+QWEN25_32B = Workload(
+    name="qwen25_32b", num_seqs=64, num_q_heads=40, num_kv_heads=8, head_dim=128,
+    block_size=16, dtype=BFLOAT16, seed=10, length_kind="uniform", lo=128, hi=4096)
+
 # Continuous batching with many live requests: 2048 sequences of U[16, 1024] tokens.
 MANY_SEQS = Workload(
     name="many_seqs", num_seqs=2048, num_q_heads=32, num_kv_heads=8, head_dim=128,
@@ -137,7 +143,8 @@ CHUNKED_PREFILL = Workload(
     prefill="chunk", chunk=512)
 
 WORKLOADS = {w.name: w for w in (TINY, LLAMA3_8B, SHARED_PREFIX, LONG_CONTEXT, RAGGED,
-                                  PREFILL, CHUNKED_PREFILL, MHA_7B, LLAMA3_405B, MANY_SEQS)}
+                                  PREFILL, CHUNKED_PREFILL, MHA_7B, LLAMA3_405B, MANY_SEQS,
+                                  QWEN25_32B)}
 
 
 # ----------------------------------------------------------------------------

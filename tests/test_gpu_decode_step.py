@@ -65,7 +65,8 @@ def _bits(t: torch.Tensor) -> torch.Tensor:
 
 CASES = ([(32, 8, bs) for bs in syn.RAGGED_BLOCK_SIZES] +
          [(8, 1, 16), (16, 2, 64), (32, 32, 16), (32, 32, 64), (64, 8, 32), (16, 16, 8),
-          (128, 8, 16), (128, 64, 16)])     # head-group passes: each writes its own heads
+          (128, 8, 16), (128, 64, 16),      # head-group passes: each writes its own heads
+          (40, 8, 16), (28, 4, 32)])        # 5 and 7 query heads per KV head
 
 
 @pytest.mark.parametrize("hq,hkv,bs", CASES)
