@@ -108,11 +108,12 @@ struct Geo {
   static constexpr int TT = kRows / H;                   // tokens per tile
   static constexpr int kQBytes = N * 256;
   // For N = 64, Q and P' are single-buffered and the room goes to a fifth ring
-  // stage (measured on GB300: long-context decode 90% -> 95% of the HBM peak).
-  // For N = 32 the same trade (six stages) measured slower (82% -> 79.5%): the
-  // softmax then waits for the previous P'.V before writing P'.
-  static constexpr int kQBufs = N >= 64 ? 1 : 2;
-  static constexpr int kPBufs = N >= 64 ? 1 : 2;
+  // stage (measured on GB300: long-context decode 90% -> 95% of the HBM peak;
+  // N = 48, 40 query heads: 0.90 -> 0.91).  For N = 32 the same trade (six
+  // stages) measured slower (82% -> 79.5%): the softmax then waits for the
+  // previous P'.V before writing P'.
+  static constexpr int kQBufs = N >= 48 ? 1 : 2;
+  static constexpr int kPBufs = N >= 48 ? 1 : 2;
   static constexpr int kPHalf = N * 256;
   static constexpr int kPBytes = 2 * kPHalf;
   // as many 32 KB ring stages as the shared memory left over allows
