@@ -770,6 +770,8 @@ def measure_stream_read(torch, pa, dev, args) -> dict:
 # Workloads measured beside the headline one in a default run.
 # The other workloads of the default line: (entry, workload, block size or None
 # for the workload's own); the ragged step at every block size it sweeps.
+PREFILL_WORKLOADS = ("prefill", "chunked_prefill", "prefill_qwen25_32b")
+
 EXTRA_WORKLOADS = (("long_context", "long_context", None), ("shared_prefix", "shared_prefix", None),
                    ("ragged", "ragged", None), ("ragged_bs8", "ragged", 8),
                    ("ragged_bs32", "ragged", 32), ("ragged_bs64", "ragged", 64),
@@ -978,7 +980,7 @@ def run_prefill(args):
     from paged_kv_cache_301_gb300 import build as _build
 
     _build.build()
-    name = args.workload if args.workload in ("prefill", "chunked_prefill") else "prefill"
+    name = args.workload if args.workload in PREFILL_WORKLOADS else "prefill"
     w = syn.WORKLOADS[name]
     cpu = None if args.no_cpu_baseline else prefill_cpu_baseline(name)
     torch.cuda.set_device(0)
@@ -1288,7 +1290,7 @@ def main():
     ap.add_argument("--workload", default="llama3_8b",
                     choices=["llama3_8b", "long_context", "shared_prefix", "ragged", "tiny",
                              "mha_7b", "llama3_405b", "many_seqs", "qwen25_32b", "prefill",
-                             "chunked_prefill"])
+                             "chunked_prefill", "prefill_qwen25_32b"])
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_head"], default="auto")
@@ -1308,7 +1310,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.op == "decode" and args.workload in ("prefill", "chunked_prefill"):
+    if args.op == "decode" and args.workload in PREFILL_WORKLOADS:
         ap.error("the prefill workloads run with --op prefill")
     if args.op != "decode":
         if args.impl == "reference":

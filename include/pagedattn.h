@@ -321,7 +321,7 @@ pa_status pa_decode_append(void* out, const void* q, void* k_pool, void* v_pool,
  * t = 0 .. position, slot_t as in pa_decode.  fp32 accumulation, output rounded
  * to the storage type.  Supported: head_dim 64 or 128, any num_q_heads /
  * num_kv_heads, block_size in {8, 16, 32, 64}, fp16 / bf16.  head_dim 128 with
- * query groups of 1, 2, 4, 8 or 16 runs on the tensor cores (tcgen05, TMA); every
+ * query groups of 1 to 8 or 16 runs on the tensor cores (tcgen05, TMA); every
  * other shape on a CUDA-core kernel.  A sequence with n_b > seq_lens[b], n_b > max_q_len,
  * seq_lens[b] > max_blocks * block_size, or rows outside [0, total_q) is skipped
  * (rows untouched; reported in checked mode); out-of-range block ids read zeros

@@ -10,7 +10,8 @@
 //
 // Work item (one CTA): sequence b, KV head h and two adjacent query tiles A, B
 // of 128 rows each = TQ = 128 / G query tokens x the G query heads of h
-// (row = token * G + g).  Every K/V tile loaded serves both, 256 query rows, so
+// (row = token * G + g; for G = 3, 5, 6, 7, 128 / G rounded down, and the last
+// 2 or 3 rows unused).  Every K/V tile loaded serves both, 256 query rows, so
 // the per-head gather (128-byte rows 2 KB apart, ~35 GB/s per SM through TMA on
 // GB300) feeds twice the tensor work of a single tile.  For KV tiles of 128 keys
 // and each query tile k:
@@ -95,6 +96,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const PrefillParams p) {
   constexpr int TQ = kRows / G;                 // query tokens per tile
+  constexpr int kUsedRows = TQ * G;             // 128, or 125 / 126 when G does not divide it
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -171,7 +173,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int s = 0; s < kStages; ++s) issued[s] = -1;
     bool ok = true, q_issued = false;
     if (lane == 0) {            // both query tiles (rows past the batch read as zeros)
-      mbar_arrive_expect_tx(&tl->q_full, 2 * kTile);
+      mbar_arrive_expect_tx(&tl->q_full, 2u * 2u * kUsedRows * 128u);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         uint8_t* dst = smem + kQOff + k * kTile;
@@ -311,7 +313,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int r = wq * 32 + lane;                // tile row = query token r / G, head r % G
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const int i = (k ? q0b : q0a) + r / G;       // query token within the sequence's queries
-    const bool row_valid = i < n;
+    // rows past TQ * G (G not a power of two) hold no query: their Q rows in
+    // shared memory are never written, and every key is masked for them
+    const bool row_valid = r < kUsedRows && i < n;
     const int pos = row_valid ? L - n + i : -1;  // keys 0 .. pos are visible
     const uint32_t scol = tmem + lane_base + k * kKeys;
     const uint32_t ocol = tmem + lane_base + 256 + k * kD;
@@ -519,7 +523,11 @@ pa_status launch_dt(int G, const PrefillParams& p, const CUtensorMap& k, const C
   switch (G) {
     case 1: return launch_g<DT, 1>(p, k, v, q, stream);
     case 2: return launch_g<DT, 2>(p, k, v, q, stream);
+    case 3: return launch_g<DT, 3>(p, k, v, q, stream);
     case 4: return launch_g<DT, 4>(p, k, v, q, stream);
+    case 5: return launch_g<DT, 5>(p, k, v, q, stream);
+    case 6: return launch_g<DT, 6>(p, k, v, q, stream);
+    case 7: return launch_g<DT, 7>(p, k, v, q, stream);
     case 8: return launch_g<DT, 8>(p, k, v, q, stream);
     case 16: return launch_g<DT, 16>(p, k, v, q, stream);
     default: return PA_ERR_UNSUPPORTED;
@@ -557,7 +565,9 @@ extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_pool, co
       (dtype != PA_FLOAT16 && dtype != PA_BFLOAT16))
     return PA_ERR_UNSUPPORTED;
   const int path = g_prefill_path;
-  const bool tc_shape = head_dim == kD && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
+  // a query tile holds 128 / G query tokens (G = 3, 5, 6, 7: 125 or 126 of its
+  // 128 rows used)
+  const bool tc_shape = head_dim == kD && ((G >= 1 && G <= 8) || G == 16);
   if (path == PA_PREFILL_TC && !tc_shape) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return PA_OK;
   if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !q_start)

@@ -137,6 +137,12 @@ PREFILL = Workload(
     block_size=16, dtype=BFLOAT16, seed=5, length_kind="uniform", lo=512, hi=4096,
     prefill="full")
 
+# The whole-prompt batch with 40 query / 8 KV heads (Qwen2.5-32B-shaped).
+PREFILL_QWEN = Workload(
+    name="prefill_qwen25_32b", num_seqs=8, num_q_heads=40, num_kv_heads=8, head_dim=128,
+    block_size=16, dtype=BFLOAT16, seed=5, length_kind="uniform", lo=512, hi=4096,
+    prefill="full")
+
 CHUNKED_PREFILL = Workload(
     name="chunked_prefill", num_seqs=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
     block_size=16, dtype=BFLOAT16, seed=6, length_kind="uniform", lo=1024, hi=8192,
@@ -144,7 +150,7 @@ CHUNKED_PREFILL = Workload(
 
 WORKLOADS = {w.name: w for w in (TINY, LLAMA3_8B, SHARED_PREFIX, LONG_CONTEXT, RAGGED,
                                   PREFILL, CHUNKED_PREFILL, MHA_7B, LLAMA3_405B, MANY_SEQS,
-                                  QWEN25_32B)}
+                                  QWEN25_32B, PREFILL_QWEN)}
 
 
 # ----------------------------------------------------------------------------

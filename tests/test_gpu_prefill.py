@@ -44,10 +44,12 @@ def _small(G, bs, dtype, lens, hkv=2):
                                num_q_heads=hkv * G, block_size=bs, dtype=dtype)
 
 
-@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8, 16])
 @pytest.mark.parametrize("bs", [8, 16, 32, 64])
 def test_whole_prompts_every_row(pa, G, bs):
-    """Lengths that end mid-block, mid-tile and exactly on tile edges."""
+    """Lengths that end mid-block, mid-tile and exactly on tile edges; every query
+    group the tensor-core kernel serves (with 3, 5, 6 or 7 query heads per KV
+    head a 128-row tile holds 42, 25, 21 or 18 query tokens)."""
     w = _small(G, bs, syn.BFLOAT16, [1, 127, 128, 300, 37])
     pb = scenarios.prefill_batch(w)
     out, dev = _run(pa, pb)
@@ -121,9 +123,11 @@ def test_deterministic_and_bad_input_reported(pa):
 
 
 @pytest.mark.parametrize("dtype", [syn.FLOAT16, syn.BFLOAT16])
-@pytest.mark.parametrize("head_dim,hq,hkv", [(64, 4, 4), (64, 12, 4), (128, 24, 4), (128, 6, 2)])
+@pytest.mark.parametrize("head_dim,hq,hkv", [(64, 4, 4), (64, 12, 4), (128, 24, 2), (128, 40, 4),
+                                             (128, 6, 2), (128, 40, 8)])
 def test_other_shapes_every_row(pa, dtype, head_dim, hq, hkv):
-    """head_dim 64 and query groups outside 1/2/4/8/16 (the CUDA-core kernel)."""
+    """head_dim 64, query groups of 10 and 12 (the CUDA-core kernel), and groups of
+    3 and 5 in fp16 and bf16."""
     w = dataclasses.replace(syn.PREFILL, name="pf_other", num_seqs=4, length_kind="fixed",
                             lens=(1, 70, 200, 33), num_q_heads=hq, num_kv_heads=hkv,
                             head_dim=head_dim, block_size=16, dtype=dtype)
