@@ -540,6 +540,48 @@ def med(xs):
     return statistics.median(xs) if xs else None
 
 
+def measure_graph(torch, step, args, dev, reps: int = 25):
+    """The K-step block captured once in a CUDA graph and replayed: the step's
+    device time without the host's per-call launch cost (which bounds the
+    latency-bound tiny workload when it is called from Python).  The library
+    allocates nothing during a call given its workspace, so the calls capture
+    as they are.  Returns a dict for the line, or one with the reason the
+    capture failed."""
+    K = args.steps
+    main = torch.cuda.current_stream()
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                step.run()
+        main.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(K):
+                step.run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            a.record(main)
+            g.replay()
+            b.record(main)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b) / K)
+        del g
+        return {"ms_per_step": round(med(ms), 5), "repeats": reps,
+                "how": f"the K = {K} steps captured once in a CUDA graph, replayed between "
+                       f"CUDA events; median over {reps} replays / K"}
+    except Exception as e:       # report, never fail the line
+        torch.cuda.synchronize()
+        return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
+
+
 def decode_entry(step, m, w, world, peak, peak_kind, args) -> dict:
     """Figures of one decode workload from its measurements."""
     K = args.steps
@@ -799,6 +841,7 @@ def run_native(args, dist_info):
                       fused=not args.split_step)
     m = measure_decode(torch, step, args, world, dev, flushed=True)
     head = decode_entry(step, m, w, world, peak, peak_kind, args)
+    head["graph"] = measure_graph(torch, step, args, dev)
     del step
     torch.cuda.empty_cache()
     workloads = {}
@@ -811,6 +854,7 @@ def run_native(args, dist_info):
             workloads[name] = decode_entry(st, measure_decode(torch, st, args, world, dev,
                                                               flushed=False),
                                            wx, world, peak, peak_kind, args)
+            workloads[name]["graph"] = measure_graph(torch, st, args, dev)
             del st
             torch.cuda.empty_cache()
         if args.kernel in ("auto", "tc"):

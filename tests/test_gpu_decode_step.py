@@ -254,3 +254,50 @@ def test_bad_arguments_raise(pa):
     assert ei.value.status == 1
     torch.cuda.synchronize()
     _pools_equal(dev, initial.k_pool, initial.v_pool)      # nothing ran
+
+
+@pytest.mark.parametrize("w", [syn.LLAMA3_8B, syn.TINY], ids=lambda w: w.name)
+def test_step_captured_in_a_cuda_graph(pa, w):
+    """A decode step with its workspace given allocates nothing, so it can be
+    captured in a CUDA graph (launch-bound loops are replayed that way); the
+    replayed step writes the same pools and outputs, bit for bit, as the eager
+    call, and matches the oracle."""
+    if w is syn.LLAMA3_8B:
+        w = dataclasses.replace(w, name="graph", num_seqs=16)
+    batch = scenarios.fixed_batch(w)
+    B = len(batch.seq_lens)
+    key_bits, val_bits = syn.token_kv_bits(w, B, sub=400_000)
+    slots = _newest_slots(batch.block_tables, batch.seq_lens, w.block_size)
+    k_ref, v_ref = batch.k_pool.copy(), batch.v_pool.copy()
+    reshape_and_cache(k_ref, v_ref, key_bits, val_bits, slots)
+    dev_e, dev_g = DeviceBatch(batch), DeviceBatch(batch)
+    key, value = to_dev(key_bits, w.dtype), to_dev(val_bits, w.dtype)
+    mx = int(batch.seq_lens.max())
+    ws = pa.workspace_for(dev_g.q, dev_g.k_pool, dev_g.tables, mx)
+
+    def step(dev, out):
+        pa.pa_decode_append(out, dev.q, dev.k_pool, dev.v_pool, key, value, dev.tables, dev.lens,
+                            w.scale, max_seq_len=mx, workspace=ws)
+
+    eager = torch.empty_like(dev_e.q)
+    step(dev_e, eager)
+    torch.cuda.synchronize()
+    out = torch.empty_like(dev_g.q)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):           # warm-up outside the capture
+        step(dev_g, out)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(dev_g, out)
+    out.zero_()
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    _pools_equal(dev_g, k_ref, v_ref)
+    _pools_equal(dev_e, k_ref, v_ref)
+    after = dataclasses.replace(batch, k_pool=k_ref, v_pool=v_ref)
+    assert_close(widen(out), scenarios.decode_f64(after), f"graph replay {w.name}")
