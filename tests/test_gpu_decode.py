@@ -128,6 +128,22 @@ def test_query_groupings(pa, hq, hkv):
     assert_close(got, scenarios.decode_f64(batch), f"Hq={hq} Hkv={hkv}")
 
 
+@pytest.mark.parametrize("hq,hkv,bs", [(40, 8, 16), (28, 4, 64), (24, 8, 8), (48, 8, 32)])
+def test_odd_query_groups_fp16(pa, hq, hkv, bs):
+    """3, 5, 6 and 7 query heads per KV head in fp16 (the grouped kernel's other
+    storage type), ragged lengths across block and tile edges."""
+    lens = (1, bs - 1, bs + 1, 129, 700, 2049)
+    w = _small("llama3_8b", num_seqs=len(lens), num_q_heads=hq, num_kv_heads=hkv,
+               block_size=bs, dtype=syn.FLOAT16, length_kind="fixed", lens=lens,
+               seed=300 + hq + bs)
+    batch = scenarios.fixed_batch(w)
+    dev = DeviceBatch(batch)
+    if pa.decode_path == "tc":
+        assert pa.decode_kernel_for(dev.q, dev.k_pool, dev.tables, 2049) == "grouped"
+    got = widen(dev.decode(pa))
+    assert_close(got, scenarios.decode_f64(batch), f"fp16 Hq={hq} Hkv={hkv} bs={bs}")
+
+
 @pytest.mark.parametrize("hkv,hq,bs,lens", [
     (8, 32, 16, (100,)),                 # fewer tiles than SMs: most CTAs idle
     (4, 16, 32, (128, 300)),
