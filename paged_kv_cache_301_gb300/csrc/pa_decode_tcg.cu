@@ -59,6 +59,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 232448 - 1024;   // per-block limit minus alignment slack
 constexpr int kStartWeight = 1;              // least start weight: a sequence start ~ one tile
+constexpr float kRescaleLog2 = 8.f;          // raise a running max only past this (base 2)
 constexpr int kWin = 640;                    // sequences of one CTA's range (shared memory)
 constexpr int kMaxSeqs = 16384;              // batch size served (also B <= (kWin - 2) grid / 2)
 
@@ -78,12 +79,14 @@ struct Tail {
   uint64_t p_full[2], p_empty[2];
   uint64_t o_full[2], o_empty[2];
   uint64_t red[2], lsum, drain;
+  uint64_t red2[2];           // second exchange of a tile whose running maxima rise
   uint64_t app_done;          // newest tokens of this CTA's sequences are in the pool
   uint64_t staged;            // final outputs staged in the ring (one arrive per softmax warp)
   uint64_t p_staged[2];       // a segment's outputs staged in P' buffer i (one arrive per softmax warp)
   uint64_t p_released[2];     // the bulk copy has read P' buffer i
   SegInfo seg[2];
   float red_buf[2][4][N];
+  alignas(16) int vote[2][4]; // per tile and softmax warp: a row exceeds its running max + 8
   float alpha[2][N];
   alignas(16) float lred[4][N];
   float m_fin[N];
@@ -220,6 +223,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       mbar_init(&tl->o_full[i], 1);
       mbar_init(&tl->o_empty[i], 4);
       mbar_init(&tl->red[i], 4);
+      mbar_init(&tl->red2[i], 4);
     }
     mbar_init(&tl->lsum, 4);
     mbar_init(&tl->drain, 1);
@@ -719,7 +723,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int r = wq * 32 + lane;            // tile row (token r / H, head r % H); O row d
     const int tt = r / H, h = lane % H;      // H divides 32
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    int tile_g = 0, seg_idx = 0, round = 0, lround = 0;
+    int tile_g = 0, seg_idx = 0, round = 0, lround = 0, rround = 0;
+    bool raised[2] = {true, true};         // per round parity: the tile moved its maxima
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, int parity) -> bool {
       const bool w = mbar_wait(bar, parity, abort_flag, kWaitNs);
@@ -779,13 +784,23 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int slot = t & 1, ph = (t >> 1) & 1;
         if (!wait_all(&tl->o_full[slot], ph)) return false;
         tc_fence_after();
-        const float* al = tl->alpha[rnd & 1];
+        if (raised[rnd & 1]) {
+          const float* al = tl->alpha[rnd & 1];
 #pragma unroll
-        for (int c0 = 0; c0 < N; c0 += 16) {
-          float o[16];
-          tmem_ld16(tmem + lane_base + 2 * N + slot * N + c0, o);
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            float o[16];
+            tmem_ld16(tmem + lane_base + 2 * N + slot * N + c0, o);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(acc[c0 + i], al[c0 + i], o[i]);
+            for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(acc[c0 + i], al[c0 + i], o[i]);
+          }
+        } else {                 // the round kept every running max: alpha = 1
+#pragma unroll
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            float o[16];
+            tmem_ld16(tmem + lane_base + 2 * N + slot * N + c0, o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[c0 + i] += o[i];
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -831,39 +846,71 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
             valid = ib < il || (ib == il && tt - ib * bx >= sh);
           }
         }
-        float wm[G];
+        bool exceed = false;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           x[g] = valid ? x[g] * p.scale_log2 : -CUDART_INF_F;
-          wm[g] = x[g];
+          exceed |= x[g] > m_run[g] + kRescaleLog2;
         }
-        // rows of the same KV head in this warp: lanes h, h+H, ... (xor H .. 16)
-#pragma unroll
-        for (int off = H; off < 32; off <<= 1)
-#pragma unroll
-          for (int g = 0; g < G; ++g) wm[g] = fmaxf(wm[g], __shfl_xor_sync(0xFFFFFFFFu, wm[g], off));
+        // Running maxima rise only where a score exceeds them by more than 2^8
+        // (always on a segment's first tile, where they are -inf): the four
+        // warps vote, and only then is the tile's max per query head reduced
+        // and every running max moved to it.  Otherwise p = 2^(s - m) may
+        // reach 2^8, which fp32 sums and the hi + lo terms of P' carry, and the
+        // accumulators need no rescale; the final division by the sum removes
+        // the choice of max.
         const int rb = round & 1;
-        if (lane < H)
-#pragma unroll
-          for (int g = 0; g < G; ++g) tl->red_buf[rb][wq][h * G + g] = wm[g];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->red[rb]);
-        if (!wait_all(&tl->red[rb], (round >> 1) & 1)) { ok = false; break; }
-        float alpha[G], pr[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const int q = h * G + g;
-          const float tm = fmaxf(fmaxf(tl->red_buf[rb][0][q], tl->red_buf[rb][1][q]),
-                                 fmaxf(tl->red_buf[rb][2][q], tl->red_buf[rb][3][q]));
-          const float m_new = fmaxf(m_run[g], tm);
-          alpha[g] = exp2f(m_run[g] - m_new);
-          pr[g] = valid ? exp2f(x[g] - m_new) : 0.f;
-          l_t[g] = fmaf(l_t[g], alpha[g], pr[g]);
-          m_run[g] = m_new;
+        {
+          const bool wv = __any_sync(0xFFFFFFFFu, exceed);
+          if (lane == 0) {
+            tl->vote[rb][wq] = wv ? 1 : 0;
+            mbar_arrive(&tl->red[rb]);
+          }
         }
-        if (wq == 0 && lane < H) {
+        if (!wait_all(&tl->red[rb], (round >> 1) & 1)) { ok = false; break; }
+        const int4 vt = *reinterpret_cast<const int4*>(tl->vote[rb]);
+        const bool raise = (vt.x | vt.y | vt.z | vt.w) != 0;
+        raised[rb] = raise;
+        float pr[G];
+        if (raise) {
+          float wm[G];
 #pragma unroll
-          for (int g = 0; g < G; ++g) tl->alpha[rb][h * G + g] = alpha[g];
+          for (int g = 0; g < G; ++g) wm[g] = x[g];
+          // rows of the same KV head in this warp: lanes h, h+H, ... (xor H .. 16)
+#pragma unroll
+          for (int off = H; off < 32; off <<= 1)
+#pragma unroll
+            for (int g = 0; g < G; ++g) wm[g] = fmaxf(wm[g], __shfl_xor_sync(0xFFFFFFFFu, wm[g], off));
+          const int rr = rround & 1;
+          if (lane < H)
+#pragma unroll
+            for (int g = 0; g < G; ++g) tl->red_buf[rr][wq][h * G + g] = wm[g];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tl->red2[rr]);
+          if (!wait_all(&tl->red2[rr], (rround >> 1) & 1)) { ok = false; break; }
+          ++rround;
+          float alpha[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const int q = h * G + g;
+            const float tm = fmaxf(fmaxf(tl->red_buf[rr][0][q], tl->red_buf[rr][1][q]),
+                                   fmaxf(tl->red_buf[rr][2][q], tl->red_buf[rr][3][q]));
+            const float m_new = fmaxf(m_run[g], tm);
+            alpha[g] = exp2f(m_run[g] - m_new);
+            pr[g] = valid ? exp2f(x[g] - m_new) : 0.f;
+            l_t[g] = fmaf(l_t[g], alpha[g], pr[g]);
+            m_run[g] = m_new;
+          }
+          if (wq == 0 && lane < H) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) tl->alpha[rb][h * G + g] = alpha[g];
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            pr[g] = valid ? exp2f(x[g] - m_run[g]) : 0.f;
+            l_t[g] += pr[g];
+          }
         }
         // P' entries of this row: (head h*G+g, column r)
         const int ps = t % Gm::kPBufs, pph = (t / Gm::kPBufs) & 1;
