@@ -193,7 +193,8 @@ int pa_decode_kernel_for(int num_seqs, int num_q_heads, int num_kv_heads, int he
  *  - Limit: a batch whose pa_decode_workspace_bytes_for(...) exceeds
  *    PA_DECODE_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE before
  *    any device work.  The grouped tensor-core kernel (the default where it
- *    serves the shape) needs at most about 11 MiB whatever the lengths; the
+ *    serves the shape) needs about 5.1 MiB per 32 query heads whatever the
+ *    lengths (batches of up to 192 query heads fit); the
  *    other kernels need [num_seqs, num_q_heads, partitions] partials, e.g.
  *    8 sequences x 64 query heads up to 128K tokens about 65 MiB, which is
  *    rejected.  Other errors are those of pa_decode.

@@ -14,9 +14,9 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 WorkspaceLayout workspace_layout(DecodeKernel k, int B, int Hq, int D, int P) {
   const size_t rows = (size_t)B * Hq * P;
   WorkspaceLayout w = {};
-  if (k == DecodeKernel::kGrouped) {      // per pass: at most kMaxHq query heads
+  if (k == DecodeKernel::kGrouped) {      // the partials of every query head
     w.sk_off = 0;
-    w.total = sk_layout(B, Hq < 64 ? Hq : 64).total;
+    w.total = sk_layout(B, Hq).total;
     return w;
   }
   size_t off = 0;

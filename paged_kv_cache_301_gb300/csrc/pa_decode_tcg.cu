@@ -136,13 +136,23 @@ constexpr int smem_bytes() {
   return Geo<H, G>::kTailOff + (int)sizeof(Tail<Geo<H, G>::N>) + 1024;
 }
 
+// Head-group passes of one call (p.head_off > 0 or p.Hkv < p.Hkv_all) run as a
+// chain: every pass but the last lets the next one launch once it has passed its
+// own dependency wait (its CTAs take the SMs as this pass's CTAs leave), and
+// every pass but the first reads only data that the first pass's wait already
+// covers, so it defers its wait to its end, where it makes its own completion
+// imply the previous pass's.
+constexpr int kChainTrigger = 1;
+constexpr int kChainLateWait = 2;
+
 struct SkParams {
   DecodeParams p;
+  int chain;                // kChainTrigger | kChainLateWait for head-group passes
   int* tile_prefix;         // [B + 1] tiles before sequence b (written by CTA 0 for the combine)
   int* weight_prefix;       // [B + 2] weight before sequence b, then the start weight (the same)
-  float* part_m;            // [grid * 2 * Hq]
+  float* part_m;            // [grid * 2][Hq_all]: each pass its own heads
   float* part_l;
-  float* part_acc;          // [grid * 2 * Hq * D]
+  float* part_acc;          // [grid * 2][Hq_all][D]
 };
 
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
@@ -255,8 +265,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
   // and waiting while this grid streams, cost this grid 0.9 us on the
   // Llama-shaped batch and 2.8 us on the long-context one (GB300, back-to-back
   // steps); triggering when the producer has issued its last copy, or at the
-  // CTA's last segment, measured in between.
-  wait_prior_grid();           // inputs may come from the previous kernel in the stream
+  // CTA's last segment, measured in between.  The next pass of a head-group
+  // chain is launched early: it cannot become resident before this pass's
+  // CTAs leave (shared memory).
+  if (!(sp.chain & kChainLateWait)) wait_prior_grid();   // inputs may come from the previous kernel
+  if (sp.chain & kChainTrigger) allow_next_grid();
   if (warp >= 2) {
     // The split (every CTA computes it; CTA 0 also stores the prefixes for the
     // combine pass), zero rows of empty sequences, length checks.  Thread et
@@ -986,7 +999,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
           }
         }
       }
-      const int64_t part0 = ((int64_t)c * 2 + sg.slot) * Hq;   // partial index of head 0
+      // partial index of this pass's head 0 (partials of all heads side by side)
+      const int64_t part0 = ((int64_t)c * 2 + sg.slot) * p.Hq_all + (int64_t)p.head_off * G;
       if (!sg.direct && wq == 0) {
         for (int q = lane; q < Hq; q += 32) {
           sp.part_m[part0 + q] = tl->m_fin[q];
@@ -1054,6 +1068,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
     tc_fence_after();
     tmem_dealloc(tmem, Gm::kTmemCols);
   }
+  if (sp.chain & kChainLateWait) wait_prior_grid();   // complete only after the previous pass
 }
 
 // Merge the partials of sequences cut by CTA range boundaries.  One warp per
@@ -1315,8 +1330,29 @@ SkLayout sk_layout(int B, int Hq) {
   return l;
 }
 
-// One pass: the KV heads p.head_off .. p.head_off + p.Hkv - 1 (of p.Hkv_all).
-static pa_status launch_pass(const DecodeParams& p, void* sk_ws, cudaStream_t stream) {
+// The stream-K area's pointers for a call over p.Hq_all query heads.
+static SkParams sk_params(const DecodeParams& p, void* sk_ws, int chain) {
+  const SkLayout l = sk_layout(p.B, p.Hq_all);
+  char* ws = static_cast<char*>(sk_ws);
+  SkParams sp;
+  sp.p = p;
+  sp.chain = chain;
+  sp.tile_prefix = reinterpret_cast<int*>(ws + l.prefix_off);
+  sp.weight_prefix = reinterpret_cast<int*>(ws + l.wprefix_off);
+  sp.part_m = reinterpret_cast<float*>(ws + l.m_off);
+  sp.part_l = reinterpret_cast<float*>(ws + l.l_off);
+  sp.part_acc = reinterpret_cast<float*>(ws + l.acc_off);
+  return sp;
+}
+
+static int launch_grid() {
+  const int grid = device_sms();
+  return grid > kSkMaxGrid ? kSkMaxGrid : grid;
+}
+
+// One pass's main kernel: the KV heads p.head_off .. p.head_off + p.Hkv - 1 (of
+// p.Hkv_all).
+static pa_status launch_pass(const DecodeParams& p, void* sk_ws, int chain, cudaStream_t stream) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return PA_ERR_UNSUPPORTED;
   const int H = p.Hkv, G = p.Hq / p.Hkv;
@@ -1354,23 +1390,18 @@ static pa_status launch_pass(const DecodeParams& p, void* sk_ws, cudaStream_t st
           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return PA_ERR_INVALID_ARG;
 
-  int grid = device_sms();
+  const int grid = launch_grid();
   if (grid <= 0) return PA_ERR_CUDA;
-  if (grid > kSkMaxGrid) grid = kSkMaxGrid;
-  const SkLayout l = sk_layout(p.B, p.Hq);
-  char* ws = static_cast<char*>(sk_ws);
-  SkParams sp;
-  sp.p = p;
-  sp.tile_prefix = reinterpret_cast<int*>(ws + l.prefix_off);
-  sp.weight_prefix = reinterpret_cast<int*>(ws + l.wprefix_off);
-  sp.part_m = reinterpret_cast<float*>(ws + l.m_off);
-  sp.part_l = reinterpret_cast<float*>(ws + l.l_off);
-  sp.part_acc = reinterpret_cast<float*>(ws + l.acc_off);
+  const SkParams sp = sk_params(p, sk_ws, chain);
+  return p.dtype == PA_BFLOAT16 ? launch_dt<PA_BFLOAT16>(H, G, sp, tk, tv, tq, grid, stream)
+                                : launch_dt<PA_FLOAT16>(H, G, sp, tk, tv, tq, grid, stream);
+}
 
-  const pa_status st = p.dtype == PA_BFLOAT16
-                           ? launch_dt<PA_BFLOAT16>(H, G, sp, tk, tv, tq, grid, stream)
-                           : launch_dt<PA_FLOAT16>(H, G, sp, tk, tv, tq, grid, stream);
-  if (st != PA_OK) return st;
+// The combine over every query head of the call (p: all heads, head_off 0).
+static pa_status launch_combine_sk(const DecodeParams& p, void* sk_ws, cudaStream_t stream) {
+  const int grid = launch_grid();
+  if (grid <= 0) return PA_ERR_CUDA;
+  const SkParams sp = sk_params(p, sk_ws, 0);
   const long long rows = (long long)p.B * p.Hq;
   if (rows == 0) return PA_OK;
   const int cgrid = (int)((rows + 3) / 4);
@@ -1394,10 +1425,11 @@ static pa_status launch_pass(const DecodeParams& p, void* sk_ws, cudaStream_t st
 
 // Query heads beyond kMaxHq (G = 16, or wide multi-head attention) run as
 // passes over groups of KV heads; the passes read disjoint heads of every pool
-// row, so the bytes read are the same as one pass over all heads.  Each pass
-// reuses the stream-K area: its main kernel starts after the previous pass's
-// combine has read it (stream order; the main kernel writes nothing before its
-// dependency wait).
+// row, so the bytes read are the same as one pass over all heads.  The passes
+// form a chain (kChainTrigger, kChainLateWait): each writes its own heads'
+// partials into the shared stream-K area (partials of all heads side by side;
+// the tile and weight prefixes are the same for every pass), so one pass can
+// start while the previous one ends, and one combine merges every head.
 pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t stream) {
   const int G = p.Hq / p.Hkv;
   const int hg = heads_per_pass(p.Hkv, G);
@@ -1407,10 +1439,11 @@ pa_status launch_decode_tcg(const DecodeParams& p, void* sk_ws, cudaStream_t str
     pp.Hkv = hg;
     pp.Hq = hg * G;
     pp.head_off = p.head_off + off;
-    const pa_status st = launch_pass(pp, sk_ws, stream);
+    const int chain = (off + hg < p.Hkv ? kChainTrigger : 0) | (off > 0 ? kChainLateWait : 0);
+    const pa_status st = launch_pass(pp, sk_ws, chain, stream);
     if (st != PA_OK) return st;
   }
-  return PA_OK;
+  return launch_combine_sk(p, sk_ws, stream);
 }
 
 }  // namespace pa
