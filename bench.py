@@ -277,13 +277,14 @@ class NativeStep:
             pa.decode_kernel_for(q, self.k_pool, tables, self.max_seq_len, partition_tokens)]
         # append_tokens, then decode: main + combine (grouped), plan + main
         # (+ combine) (per-head), main (+ combine) (CUDA cores).  The fused step
-        # (pa_decode_append) writes the new tokens inside the grouped main kernel.
+        # (pa_decode_append) writes the new tokens inside the grouped and the
+        # CUDA-core main kernels.
         if self.kernel == "tcg":
             self.launches_per_step = (0 if fused else 1) + 2
         elif self.kernel == "tc_head":
             self.launches_per_step = 1 + 2 + (1 if P > 1 else 0)
         else:
-            self.launches_per_step = 1 + 1 + (1 if P > 1 else 0)
+            self.launches_per_step = (0 if fused else 1) + 1 + (1 if P > 1 else 0)
         if pairs:                       # copy-on-write block copies
             self.launches_per_step += 1
         # Every step's inputs (q, the new tokens' K/V, tables, lengths,
@@ -330,7 +331,8 @@ class NativeStep:
 
     def decode(self, s: int = 0):
         """The decode call; with `fused`, pa_decode_append, which also writes the
-        step's new tokens (inside the grouped kernel, else as a launch before it)."""
+        step's new tokens (inside the grouped and CUDA-core kernels, else as a launch
+        before it)."""
         v = self.bufs[s]
         if self.fused:
             self.pa.pa_decode_append(v["out"], v["q"], self.k_pool, self.v_pool, v["key"],
@@ -621,7 +623,7 @@ def decode_entry(step, m, w, world, peak, peak_kind, args) -> dict:
                        "tc_head": "(plan + split-K main + combine)" + (
                            ", after the cache write" if step.fused else ""),
                        "simt": "(split-K main + combine)" + (
-                           ", after the cache write" if step.fused else "")}[step.kernel],
+                           ", cache write inside the main kernel" if step.fused else "")}[step.kernel],
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

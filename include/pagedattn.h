@@ -293,7 +293,9 @@ pa_status pa_append_tokens(void* k_pool, void* v_pool, const void* key, const vo
  * of pa_decode (key and value 16-byte aligned).  Where pa_decode runs its
  * grouped tensor-core kernel, the write happens inside it: the CTA that reads a
  * sequence's last tile stores the newest token before loading that tile, which
- * saves one launch per step.  The block receiving a sequence's newest token must
+ * saves one launch per step.  The CUDA-core kernel writes it inside too (one
+ * CTA per sequence and KV head stores the row; every CTA reads that token from
+ * key / value); with the per-head tensor-core kernel it is a launch before it.  The block receiving a sequence's newest token must
  * not be in another sequence's table (copy-on-write it first, as for any write).
  */
 pa_status pa_decode_append(void* out, const void* q, void* k_pool, void* v_pool,

@@ -149,7 +149,7 @@ extern "C" int pa_decode_kernel_for(int num_seqs, int num_q_heads, int num_kv_he
 
 // pa_decode, optionally preceded by the decode-step cache write of
 // pa_append_tokens (new_k / new_v non-null): fused into the grouped tensor-core
-// kernel where that kernel runs, two launches otherwise.  Every argument is
+// kernel and into the CUDA-core kernel, two launches with the per-head kernel.  Every argument is
 // checked before anything is launched.
 static pa_status decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool,
                              const void* new_k, const void* new_v,
@@ -198,11 +198,14 @@ static pa_status decode_impl(void* out, const void* q, const void* k_pool, const
   }
   const bool per_head = kernel == DecodeKernel::kPerHead;
   const int P = p.P;
-  if (append) {
+  if (append && per_head) {
     st = pa_append_tokens(const_cast<void*>(k_pool), const_cast<void*>(v_pool), new_k, new_v,
                           block_tables, seq_lens, nullptr, num_seqs, 0, num_kv_heads, head_dim,
                           block_size, max_blocks, num_blocks, dtype, status_dev, stream);
     if (st != PA_OK) return st;
+  } else if (append) {          // the CUDA-core kernel writes the newest tokens itself
+    p.new_k = new_k;
+    p.new_v = new_v;
   }
   if (per_head) {
     st = launch_decode_tc(p, reinterpret_cast<int2*>(ws + wl.items_off),

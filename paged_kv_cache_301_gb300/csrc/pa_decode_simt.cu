@@ -81,6 +81,38 @@ decode_simt_kernel(const DecodeParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int L = clamp_len(p, b, part == 0 && blockIdx.y == 0 && tid == 0);
   const int hq0 = h * G + g0;
+  const int32_t* table = p.block_tables + (int64_t)b * p.max_blocks;
+  // Decode-step cache write (pa_decode_append: new_k / new_v non-null): the CTA
+  // of partition 0 and the first query-head chunk of each (sequence, KV head)
+  // stores head h of the newest token, position seq_lens[b] - 1, in its slot
+  // (nothing for a length of 0, or past the table; a bad block id is reported);
+  // every CTA that reads that token takes it from new_k / new_v, so no CTA reads
+  // a slot while it is written.
+  int newest = -1;
+  if (p.new_k != nullptr) {
+    const int L_raw = p.seq_lens[b];
+    if (L_raw == L) newest = L - 1;
+    if (part == 0 && g0 == 0) {
+      if (L_raw > 0 && L_raw <= p.max_blocks * p.bs) {
+        const int pos = L_raw - 1;
+        const int32_t blk = table[pos / p.bs];
+        if (blk < 0 || blk >= p.num_blocks) {
+          if (tid == 0) report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+        } else {
+          const int64_t dst = (((int64_t)blk * p.bs + pos % p.bs) * p.Hkv + h) * D;
+          const int64_t src = ((int64_t)b * p.Hkv + h) * D;
+          for (int v = tid; v < D / VEC; v += 128) {
+            reinterpret_cast<uint4*>(const_cast<void*>(p.k_pool))[dst / VEC + v] =
+                reinterpret_cast<const uint4*>(p.new_k)[src / VEC + v];
+            reinterpret_cast<uint4*>(const_cast<void*>(p.v_pool))[dst / VEC + v] =
+                reinterpret_cast<const uint4*>(p.new_v)[src / VEC + v];
+          }
+        }
+      } else if (L_raw != 0 && tid == 0) {
+        report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
+      }
+    }
+  }
   if (L == 0) {   // empty context: a zero output row (+0.0 in fp16 and bf16)
     if (part == 0)
       for (int o = tid; o < gn * D; o += 128)
@@ -114,8 +146,8 @@ decode_simt_kernel(const DecodeParams p) {
     }
   }
 
-  const int32_t* table = p.block_tables + (int64_t)b * p.max_blocks;
   const int64_t slot_elems = (int64_t)p.Hkv * D;
+  const int64_t new_row = ((int64_t)b * p.Hkv + h) * D + li * VEC;   // newest token, head h
   const uint16_t* kbase = static_cast<const uint16_t*>(p.k_pool) + (int64_t)h * D + li * VEC;
   const uint16_t* vbase = static_cast<const uint16_t*>(p.v_pool) + (int64_t)h * D + li * VEC;
   float* s_scores = smem;
@@ -133,7 +165,8 @@ decode_simt_kernel(const DecodeParams p) {
         if (checked && (blk < 0 || blk >= p.num_blocks)) {
           report(p.status_dev, PA_ERR_BAD_BLOCK_ID);
         } else {
-          kv[u] = load_nc(kbase + (((int64_t)blk << bs_shift) + (t & bs_mask)) * slot_elems);
+          kv[u] = t == newest ? load_nc(static_cast<const uint16_t*>(p.new_k) + new_row)
+                              : load_nc(kbase + (((int64_t)blk << bs_shift) + (t & bs_mask)) * slot_elems);
         }
       }
     }
@@ -201,7 +234,8 @@ decode_simt_kernel(const DecodeParams p) {
         const int t = start + tl;
         const int32_t blk = table[t >> bs_shift];
         if (!checked || (blk >= 0 && blk < p.num_blocks))
-          vv[u] = load_nc(vbase + (((int64_t)blk << bs_shift) + (t & bs_mask)) * slot_elems);
+          vv[u] = t == newest ? load_nc(static_cast<const uint16_t*>(p.new_v) + new_row)
+                              : load_nc(vbase + (((int64_t)blk << bs_shift) + (t & bs_mask)) * slot_elems);
       }
     }
 #pragma unroll
