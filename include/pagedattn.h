@@ -144,7 +144,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
  *     all KV heads at once, over an equal share of the batch's tokens;
  *     head_dim 128, num_q_heads / num_kv_heads in {1,2,4,8,16} (or 3, 5, 6, 7
  *     when num_kv_heads is a multiple of 4: passes of 4 or 8 KV heads),
- *     num_seqs <= 16384; more than 64 query heads run as passes over groups of
+ *     num_seqs <= 32768; more than 64 query heads run as passes over groups of
  *     1-32 KV heads (a group must divide num_kv_heads);
  *   per-head tensor-core kernel (tcgen05 + TMA): one KV head per work item;
  *     head_dim 128, any grouping;

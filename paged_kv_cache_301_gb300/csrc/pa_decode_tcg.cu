@@ -61,7 +61,7 @@ constexpr int kSmemBudget = 232448 - 1024;   // per-block limit minus alignment 
 constexpr int kStartWeight = 1;              // least start weight: a sequence start ~ one tile
 constexpr float kRescaleLog2 = 8.f;          // raise a running max only past this (base 2)
 constexpr int kWin = 640;                    // sequences of one CTA's range (shared memory)
-constexpr int kMaxSeqs = 16384;              // batch size served (also B <= (kWin - 2) grid / 2)
+constexpr int kMaxSeqs = 32768;              // batch size served (also B <= (kWin - 2) grid / 2)
 
 
 struct SegInfo {

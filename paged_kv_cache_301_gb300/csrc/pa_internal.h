@@ -59,7 +59,7 @@ pa_status launch_decode_tc(const DecodeParams& p, int2* items, int* queue, cudaS
 
 // Tensor-core path, all KV heads of a block per CTA with a stream-K split
 // (head_dim 128, G in {1,2,4,8,16}, or 3, 5, 6, 7 in passes of 4 or 8 KV
-// heads; up to 16384 sequences): main + combine,
+// heads; up to 32768 sequences): main + combine,
 // once per group of KV heads with at most 64 query heads.
 constexpr int kSkMaxGrid = 160;          // persistent CTAs at most (GB300: 152 SMs)
 struct SkLayout {

@@ -366,22 +366,24 @@ def test_workspace_of_exactly_the_grouped_kernels_size(pa):
     assert e.value.status == 3
 
 
-def test_ten_thousand_tiny_sequences(pa):
-    """10,000 sequences of 1-8 tokens: each CTA's range meets ~66 sequences (the
-    grouped kernel's shared-memory window), most CTA boundaries fall between
-    sequences; sampled rows against the oracle, every row finite."""
+@pytest.mark.parametrize("B", [10000, 20000])
+def test_ten_thousands_of_tiny_sequences(pa, B):
+    """10,000 and 20,000 sequences of 1-8 tokens: each CTA's range meets ~66 or
+    ~130 sequences (the grouped kernel's shared-memory window), most CTA
+    boundaries fall between sequences; sampled rows against the oracle, every
+    row finite."""
     if pa.decode_path == "simt":
         pytest.skip("the grouped kernel's window; the CUDA-core kernel is covered elsewhere")
-    B = 10000
-    w = _small("llama3_8b", num_seqs=B, length_kind="uniform", lo=1, hi=8, seed=4242)
+    w = _small("llama3_8b", num_seqs=B, length_kind="uniform", lo=1, hi=8, seed=4242 + B)
     batch = scenarios.fixed_batch(w, fill_all=True)
     dev = DeviceBatch(batch)
     if pa.decode_path == "tc":
         assert pa.decode_kernel_for(dev.q, dev.k_pool, dev.tables, 8) == "grouped"
     got = widen(dev.decode(pa, max_seq_len=8))
     assert np.isfinite(got).all()
-    rows = sorted(set(list(range(0, B, 97)) + list(range(4990, 5030)) + [B - 1]))
-    assert_close(got[rows], scenarios.decode_f64(batch, sequences=rows)[rows], "B=10000")
+    mid = B // 2
+    rows = sorted(set(list(range(0, B, 97)) + list(range(mid - 10, mid + 30)) + [B - 1]))
+    assert_close(got[rows], scenarios.decode_f64(batch, sequences=rows)[rows], f"B={B}")
 
 
 @pytest.mark.parametrize("hq,hkv,lens", [
