@@ -174,11 +174,12 @@ def gpu_uuid(torch, dev) -> str | None:
 # native arm
 # ----------------------------------------------------------------------------
 
-# The device code of the grouped decode kernel: its template, the parameter
-# struct it reads, and the device headers it includes (host-side launch code is
-# left out, so a change there keeps the recorded counters).
+# The device code of the grouped decode kernel: its constants and tile
+# geometry, its template, the parameter structs it reads, and the device headers
+# it includes (host-side launch code is left out, so a change there keeps the
+# recorded counters).
 DECODE_KERNEL_TEXT = (
-    ("pa_decode_tcg.cu", "__device__ __forceinline__ int clamp_len", "// Merge the partials"),
+    ("pa_decode_tcg.cu", "constexpr int kD = 128;", "// Merge the partials"),
     ("pa_internal.h", "struct DecodeParams {", "};"),
     ("pa_common.cuh", None, None),
     ("pa_sm100.cuh", None, None),

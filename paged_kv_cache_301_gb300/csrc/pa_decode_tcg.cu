@@ -19,8 +19,9 @@
 //
 // Work split (stream-K): the batch is a sequence of token tiles, each sequence
 // padded to whole tiles.  A sequence weighs a start weight sw + its tiles
-// (starting a sequence costs a CTA about one tile's time: its epilogue and the
-// next sequence's first copies, so sw = 1), and CTA c of the persistent grid
+// (starting a sequence costs a CTA its epilogue, the next Q and the refill of
+// its pipeline: about one tile's time with two Q / P' buffers, three with one,
+// so sw = 1 or 3), and CTA c of the persistent grid
 // takes the tiles whose weighted positions fall in [c*W/grid, (c+1)*W/grid), W
 // the batch's total weight.  Every CTA gets the same weight to within one,
 // whatever the length mix.  A sequence that lies inside one CTA's range is
@@ -58,7 +59,6 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 232448 - 1024;   // per-block limit minus alignment slack
-constexpr int kStartWeight = 1;              // least start weight: a sequence start ~ one tile
 constexpr float kRescaleLog2 = 8.f;          // raise a running max only past this (base 2)
 constexpr int kWin = 640;                    // sequences of one CTA's range (shared memory)
 constexpr int kMaxSeqs = 32768;              // batch size served (also B <= (kWin - 2) grid / 2)
@@ -117,6 +117,13 @@ struct Geo {
   // previous P'.V before writing P'.
   static constexpr int kQBufs = N >= 48 ? 1 : 2;
   static constexpr int kPBufs = N >= 48 ? 1 : 2;
+  // Least start weight of a sequence, in tiles.  With one Q / P' buffer the
+  // next sequence's Q and first scores wait for the previous one's last tile,
+  // so nothing of a sequence start overlaps; on GB300 a weight of 3 measured
+  // best there (Llama-3-405B-shaped, N = 64: 109.7 -> 104.8 us per step; 40
+  // query heads, N = 48: 101.3 -> 97.7 us), and 1 with two buffers (N = 32:
+  // 97.9 us at 1, 98.4 at 3).
+  static constexpr int kStartWeight = kQBufs == 1 ? 3 : 1;
   static constexpr int kPHalf = N * 256;
   static constexpr int kPBytes = 2 * kPHalf;
   // as many 32 KB ring stages as the shared memory left over allows
@@ -309,10 +316,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_k,
       T += tl->scan[0][w];
       NE += tl->scan[1][w];
     }
-    // start weight: the least >= kStartWeight with (T + sw NE) / grid + 1 <=
+    // start weight: the least >= Gm::kStartWeight with (T + sw NE) / grid + 1 <=
     // (kWin - 2)(sw + 1), so that no range meets more than kWin sequences (the
     // host keeps NE <= (kWin - 2) grid / 2, so den > 0)
-    int sw = kStartWeight;
+    int sw = Gm::kStartWeight;
     {
       const long long num = (long long)T + grid - (long long)(kWin - 2) * grid;
       const long long den = (long long)(kWin - 2) * grid - NE;
@@ -1308,8 +1315,8 @@ bool tcg_supported(const DecodeParams& p) {
   if ((long long)p.num_blocks * p.bs + 64 >= (1ll << 31)) return false;
   if ((long long)p.B * p.Hq >= (1ll << 31)) return false;
   // The start weight keeps every range within its window when B <= (kWin - 2)
-  // grid / 2; it is then at most T / den + 1 with den >= B, so the batch's
-  // weight T + sw B <= 2 T + B stays an int.
+  // grid / 2; it is then at most max(3, T / den + 1) with den >= B, so the
+  // batch's weight T + sw B <= max(T + 3 B, 2 T + B) stays an int.
   const int grid = device_sms() < kSkMaxGrid ? device_sms() : kSkMaxGrid;
   if (grid <= 0 || 2ll * p.B > (long long)(kWin - 2) * grid) return false;
   const long long TT = kRows / hg;
