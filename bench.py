@@ -820,6 +820,8 @@ PREFILL_WORKLOADS = ("prefill", "chunked_prefill", "prefill_qwen25_32b")
 EXTRA_WORKLOADS = (("long_context", "long_context", None), ("shared_prefix", "shared_prefix", None),
                    ("ragged", "ragged", None), ("ragged_bs8", "ragged", 8),
                    ("ragged_bs32", "ragged", 32), ("ragged_bs64", "ragged", 64),
+                   ("many_seqs", "many_seqs", None), ("mha_7b", "mha_7b", None),
+                   ("qwen25_32b", "qwen25_32b", None), ("llama3_405b", "llama3_405b", None),
                    ("tiny", "tiny", None))
 
 

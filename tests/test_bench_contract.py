@@ -48,11 +48,13 @@ def test_native_arm_line():
     assert d["gpu_launches"] == 2 * 20 * d["repeats"]
     # every other decode workload, prefill and the read stream in the same line
     assert {"long_context", "shared_prefix", "ragged", "ragged_bs8", "ragged_bs32", "ragged_bs64",
-            "tiny", "prefill"} <= set(d["workloads"])
+            "many_seqs", "mha_7b", "qwen25_32b", "llama3_405b", "tiny", "prefill"} <= \
+        set(d["workloads"])
     assert d["workloads"]["tiny"]["ms_per_step"] > 0         # latency-bound: no roofline target
     # the same steps replayed from a CUDA graph (the host's launch cost left out)
     assert d["graph"]["ms_per_step"] > 0 and d["workloads"]["tiny"]["graph"]["ms_per_step"] > 0
-    for name in ("long_context", "shared_prefix", "ragged", "ragged_bs8", "ragged_bs32", "ragged_bs64"):
+    for name in ("long_context", "shared_prefix", "ragged", "ragged_bs8", "ragged_bs32", "ragged_bs64",
+                 "many_seqs", "mha_7b", "qwen25_32b", "llama3_405b"):
         x = d["workloads"][name]
         assert x["config"]["workload"] == name and x["value"] > 0 and x["tokens_per_s"] > 0
         assert x["roofline"]["bound"] == "hbm" and 0 < x["roofline"]["frac"] < 1.5
